@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the HyTopK hot path on one GB300 (or N independent GPUs).
+
+One step = hytopk_select over the workload (sampled threshold, fused
+score + filter, check, exact select/sort, recovery) followed by
+hytopk_replay of the selected indices. The default workload is the
+GLM-5.1-like slice of the HyScale explainer's worked example: L = 2^20 keys,
+n = 8192 queries at the last positions, H = 64, d = 128, k = 2048, fp8 e4m3
+inputs with fp32 scales (synthetic, seeded).
+
+Prints ONE JSON line (rank 0). `value` is scored causal query-key pairs per
+second over the whole step (select + replay), summed over ranks.
+
+Timing: W warm-up steps, then exactly K steps between a barrier +
+synchronize on both sides, CUDA events on the launching stream, max over
+ranks. The inputs of a step (K 128 MiB + Q 64 MiB + the 1 GiB candidate
+buffer) exceed the 129 MB L2, so no flush is added between steps.
+
+--impl reference times the CPU oracle (test infrastructure, the baseline
+arm) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic_inputs as si  # noqa: E402
+
+METRIC = ("indexer q-k pairs/s + exact top-k at 1M ctx (% TC peak); "
+          "replay entries/s (% HBM)")
+REPLAY_BYTES_PER_ENTRY = {  # idx 4 + key row d*esize + key scale + out 4 + q/w share
+    "e4m3": 4 + 128 + 4 + 4 + 4.25, "bf16": 4 + 256 + 4 + 4.25}
+WORKLOADS = {"glm_1m": si.glm_1m, "mixed_contexts": si.mixed_contexts,
+             "tiny_exact": si.tiny_exact}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="hytopk", choices=["hytopk", "reference"])
+    ap.add_argument("--workload", default="glm_1m", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-twopass", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=48, help="oracle sample size (queries)")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "hytopk" else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def pairs_of(case):
+    return int((case["positions"].astype(np.int64) + 1).sum())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ---- clocks during the timed region ---------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        for line in open(self.file.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "util": float(parts[4]), "hw": parts[6], "hwt": parts[7],
+                             "swt": parts[8], "pcap": parts[9]})
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [r for r in rows if r["util"] >= 50] or rows
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                          ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if any(r[key] == "Active" for r in busy):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["max"] for r in busy), "reasons": reasons,
+                "samples": len(busy)}
+
+
+# ---- the CPU oracle (baseline arm and cpu_baseline) -------------------------------------
+
+def oracle_sample(case, rows):
+    import oracle
+
+    sub_pairs = int((case["positions"][rows].astype(np.int64) + 1).sum())
+    t0 = time.perf_counter()
+    oracle.select(case, rows=rows)
+    dt = time.perf_counter() - t0
+    return sub_pairs, dt
+
+
+def cpu_baseline(case, n_rows):
+    rows = si.sampled_rows(len(case["positions"]), n_rows)
+    pairs, dt = oracle_sample(case, rows)
+    return {"value": pairs / dt, "unit": "pairs/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"oracle select of {len(rows)} of {len(case['positions'])} queries "
+                      f"({pairs} causal pairs) of {case['name']}, {dt:.1f} s, OpenMP over "
+                      "queries on all host cores"}
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    case = WORKLOADS[args.workload]()
+    rows = si.sampled_rows(len(case["positions"]), min(16, len(case["positions"])))
+    for _ in range(args.warmup):
+        oracle_sample(case, rows)
+    tot_pairs, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        p, dt = oracle_sample(case, rows)
+        tot_pairs += p
+        tot_t += dt
+    value = tot_pairs / tot_t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "pairs/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": case["dtype"],
+            "data": "synthetic", "config": workload_config(case),
+            "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"each step: oracle select of {len(rows)} queries"},
+            "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(case):
+    n, H, d = case["q"].shape
+    return {"workload": case["name"], "L": int(case["k"].shape[0]), "n": int(n), "H": int(H),
+            "d": int(d), "k_top": int(case["k_top"]), "capacity": 8 * int(case["k_top"]),
+            "positions": "last n" if case["name"] == "glm_1m" else "see synthetic_inputs",
+            "l2": "inputs larger than L2 (K 128 MiB + Q 64 MiB + 1 GiB candidate buffer per step)"}
+
+
+# ---- the GPU arm -------------------------------------------------------------------------
+
+def launches_per_step(dtype):
+    # select: rank, pack, [key-scale check], threshold, filter, check, select, recover;
+    # then one replay launch
+    return (8 if dtype == "e4m3" else 7) + 1
+
+
+def gpu_arm(args, world, rank, local):
+    import torch
+
+    import exact_top_token_gb300 as hk
+
+    hk.build()
+    hk.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = WORKLOADS[args.workload]()
+    n, H, d = case["q"].shape
+    L = case["k"].shape[0]
+    k_top = case["k_top"]
+    pairs = pairs_of(case)
+    t = si.to_torch(case, dev)
+    dt_code = hk.E4M3 if case["dtype"] == "e4m3" else hk.BF16
+    ws = torch.empty(hk.select_workspace_size(n, L, H, d, k_top, 0, dt_code), dtype=torch.uint8,
+                     device=dev)
+    idx = torch.empty((n, k_top), dtype=torch.int32, device=dev)
+    sc = torch.empty((n, k_top), dtype=torch.float32, device=dev)
+    rs = torch.empty((n, k_top), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nph = len(hk.PHASES) + 1
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
+                   for _ in range(args.steps)]
+
+    def step(events=None):
+        hk.select(t["q"], t["k"], t["w"], t["positions"], k_top, q_scale=t["q_scale"],
+                  k_scale=t["k_scale"], workspace=ws, out=(idx, sc),
+                  phase_events=None if events is None else events[:nph])
+        hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"],
+                  out=rs)
+        if events is not None:
+            events[nph].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(step_events[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if rank == 0 else None
+    ms_total = max_over_ranks(start.elapsed_time(stop), world, dev)
+    ms_step = ms_total / args.steps
+    phase_ms = {name: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_events)
+                for j, name in enumerate(hk.PHASES)}
+    replay_ms = statistics.mean(ev[nph - 1].elapsed_time(ev[nph]) for ev in step_events)
+    select_ms = statistics.mean(ev[0].elapsed_time(ev[nph - 1]) for ev in step_events)
+
+    # correctness guard: replay reproduces the selected scores bit for bit
+    if not torch.equal(rs, sc):
+        raise RuntimeError("replayed scores differ from the selected scores")
+
+    pk = peaks()
+    flops_per_pair = 2 * H * d
+    filter_s = phase_ms["filter"] / 1e3
+    achieved_tflops = pairs * flops_per_pair / filter_s / 1e12
+    # first version scores on the CUDA cores: fp32 FMA roofline (152 SMs x 128 lanes x 2 flop)
+    alu_peak = 152 * 128 * 2 * (clk["sm_max_mhz"] if clk and clk.get("sm_max_mhz") else 2070) / 1e6
+    roofline = {"kernel": "k_filter (fused score + threshold filter)", "bound": "alu",
+                "achieved": achieved_tflops, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved_tflops / alu_peak, "traffic": None,
+                "algorithmic_flops_per_launch": pairs * flops_per_pair,
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock",
+                "tensor_frac_fp8_of_measured": achieved_tflops / (2 * pk["bf16_tflops"])}
+    replay_bytes = n * k_top * REPLAY_BYTES_PER_ENTRY[case["dtype"]]
+    replay = {"entries_per_s": n * k_top / (replay_ms / 1e3), "ms": replay_ms,
+              "achieved_gbs": replay_bytes / (replay_ms / 1e3) / 1e9,
+              "frac_hbm_of_measured": replay_bytes / (replay_ms / 1e3) / 1e9 / pk["hbm_gbs"]}
+
+    line = {"metric": METRIC, "value": world * pairs / (ms_step / 1e3), "unit": "pairs/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": case["dtype"], "data": "synthetic", "config": workload_config(case),
+            "clocks": clk, "gpu_launches": launches_per_step(case["dtype"]) * args.steps,
+            "roofline": roofline, "select_ms": select_ms, "phases_ms": phase_ms,
+            "replay": replay, "peaks": pk}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, hk, case, dev, ws, world)
+    if not args.no_twopass:
+        line["twopass"] = twopass(hk, case, t, dev, idx, pairs)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e(args, hk, case, dev, ws, world):
+    """Same step through the public API with pinned host inputs: host-to-device
+    copies of every input and device-to-host reads of idx and replay scores are
+    inside the timed region."""
+    import torch
+
+    host = {}
+    for key in ("q", "k", "q_scale", "k_scale", "w", "positions"):
+        a = case[key]
+        host[key] = None if a is None else torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    n, H, d = case["q"].shape
+    k_top = case["k_top"]
+    out_idx = torch.empty((n, k_top), dtype=torch.int32).pin_memory()
+    out_rs = torch.empty((n, k_top), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = out_idx.numel() * 4 + out_rs.numel() * 4
+
+    def run():
+        dv = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in host.items()}
+        if case["dtype"] == "bf16":
+            q = dv["q"].view(torch.int16).view(torch.bfloat16)
+            k = dv["k"].view(torch.int16).view(torch.bfloat16)
+        else:
+            q = dv["q"].view(torch.float8_e4m3fn)
+            k = dv["k"].view(torch.float8_e4m3fn)
+        idx, sc, _ = hk.select(q, k, dv["w"], dv["positions"], k_top, q_scale=dv["q_scale"],
+                               k_scale=dv["k_scale"], scores=False, workspace=ws)
+        rs = hk.replay(q, k, dv["w"], idx, q_scale=dv["q_scale"], k_scale=dv["k_scale"])
+        out_idx.copy_(idx, non_blocking=True)
+        out_rs.copy_(rs, non_blocking=True)
+
+    steps = max(1, min(args.steps, 3))
+    run()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        run()
+    torch.cuda.synchronize()
+    dt = max_over_ranks((time.perf_counter() - t0) / steps, world, dev)
+    return {"value": world * pairs_of(case) / dt, "unit": "pairs/s", "ms_per_step": dt * 1e3,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def twopass(hk, case, t, dev, idx_ref, pairs):
+    """The in-library materialise-then-top-k path, timed once after a warm-up."""
+    import torch
+
+    n, H, d = case["q"].shape
+    L = case["k"].shape[0]
+    dt_code = hk.E4M3 if case["dtype"] == "e4m3" else hk.BF16
+    free, _ = torch.cuda.mem_get_info(dev)
+    full = hk.twopass_workspace_size(n, L, H, d, case["k_top"], dt_code, 0)
+    rows = n if full < 0.8 * free else max(1, int(0.6 * free) // (L * 4))
+    wsz = hk.twopass_workspace_size(n, L, H, d, case["k_top"], dt_code, rows)
+    ws2 = torch.empty(wsz, dtype=torch.uint8, device=dev)
+
+    def run():
+        return hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], case["k_top"],
+                                 q_scale=t["q_scale"], k_scale=t["k_scale"], workspace=ws2)
+
+    run()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    i2, _ = run()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    same = bool(torch.equal(i2, idx_ref))
+    del ws2
+    return {"value": pairs / (ms / 1e3), "unit": "pairs/s", "ms": ms, "rows_per_chunk": rows,
+            "table_bytes_written": n * L * 4, "same_idx_as_hytopk": same}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+    else:
+        gpu_arm(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,262 @@
+// api.cu -- the C ABI of the library (include/hytopk.h): argument checks,
+// workspace layout and the launch sequence. Nothing here synchronises the
+// stream or allocates memory.
+#include <cstdint>
+#include <cstring>
+
+#include "launch.h"
+
+using namespace hytopk;
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool supported_h(int H) { return H >= 1 && H <= 128 && (H & (H - 1)) == 0; }
+bool supported_d(int d) { return d == 64 || d == 128; }
+int elem_size(hytopk_dtype dt) { return dt == HYTOPK_BF16 ? 2 : 1; }
+bool valid_dtype(hytopk_dtype dt) { return dt == HYTOPK_BF16 || dt == HYTOPK_E4M3; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every entry point.
+hytopk_status check_shape(int n, int L, int H, int d, int k_top, hytopk_dtype dt) {
+  if (n < 0 || L < 1 || H < 1 || d < 1 || k_top < 1 || !valid_dtype(dt)) return HYTOPK_INVALID_ARG;
+  if (!supported_h(H) || !supported_d(d) || k_top > kMaxTopK) return HYTOPK_UNSUPPORTED;
+  if (n > (1 << 22) || L > (1 << 30)) return HYTOPK_UNSUPPORTED;
+  return HYTOPK_OK;
+}
+
+hytopk_status check_inputs(const void* q, const float* q_scale, const void* k, const float* k_scale,
+                           const float* w, hytopk_dtype dt, int n) {
+  if (!k) return HYTOPK_INVALID_ARG;
+  if (n > 0 && (!q || !w)) return HYTOPK_INVALID_ARG;
+  if (dt == HYTOPK_E4M3) {
+    if (!k_scale || (n > 0 && !q_scale)) return HYTOPK_INVALID_ARG;
+  } else if (q_scale || k_scale) {
+    return HYTOPK_INVALID_ARG;
+  }
+  const void* ptrs[] = {q, q_scale, k, k_scale, w};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return HYTOPK_MISALIGNED;
+  return HYTOPK_OK;
+}
+
+int pad_queries(int n) { return (n + kQueryPad - 1) / kQueryPad * kQueryPad; }
+
+struct SelectLayout {
+  size_t perm, qpos, wq, qp, thr, cnt, cand, flist, failed, ctr, rowbuf, rowlist, total;
+};
+
+SelectLayout select_layout(int n, int L, int H, int d, int C, hytopk_dtype dt) {
+  const size_t np = (size_t)pad_queries(n);
+  SelectLayout s{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 1024);
+    return at;
+  };
+  s.ctr = take(kCtrCount * sizeof(uint32_t));
+  s.perm = take(np * 4);
+  s.qpos = take(np * 4);
+  s.thr = take(np * 4);
+  s.cnt = take(np * 4);
+  s.flist = take(np * 4);
+  s.failed = take(np);
+  s.wq = take(np * H * 4);
+  s.qp = take(np * H * d * elem_size(dt));
+  s.cand = take(np * (size_t)C * 8);
+  s.rowbuf = take((size_t)kRecoveryCtas * L * 4);
+  s.rowlist = take((size_t)kRecoveryCtas * L * 8);
+  s.total = off;
+  return s;
+}
+
+int default_capacity(int k_top, int capacity) { return capacity > 0 ? capacity : 8 * k_top; }
+
+Problem make_problem(const void* q, const float* q_scale, const void* k, const float* k_scale,
+                     const float* w, const int32_t* positions, int n, int L, int H, int d,
+                     int k_top, hytopk_dtype dt) {
+  Problem p;
+  p.q = q;
+  p.q_scale = q_scale;
+  p.k = k;
+  p.k_scale = k_scale;
+  p.w = w;
+  p.positions = positions;
+  p.n = n;
+  p.L = L;
+  p.H = H;
+  p.d = d;
+  p.k_top = k_top;
+  p.dt = dt == HYTOPK_E4M3 ? 1 : 0;
+  return p;
+}
+
+#define HYTOPK_TRY(expr)                          \
+  do {                                            \
+    cudaError_t e_ = (expr);                      \
+    if (e_ != cudaSuccess) return HYTOPK_CUDA_ERROR; \
+  } while (0)
+
+hytopk_status record(const hytopk_select_options* opts, int phase, cudaStream_t st) {
+  if (opts && opts->phase_events && opts->phase_events[phase])
+    if (cudaEventRecord(opts->phase_events[phase], st) != cudaSuccess) return HYTOPK_CUDA_ERROR;
+  return HYTOPK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
+                                    hytopk_dtype dt) {
+  if (check_shape(n, L, H, d, k_top, dt) != HYTOPK_OK) return 0;
+  const int C = default_capacity(k_top, capacity);
+  if (capacity < 0 || C < k_top) return 0;
+  return select_layout(n, L, H, d, C, dt).total;
+}
+
+hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* k,
+                               const float* k_scale, const float* w, const int32_t* positions,
+                               int n, int L, int H, int d, int k_top, hytopk_dtype dt,
+                               int32_t* idx_out, float* scores_out, int capacity,
+                               void* workspace, size_t workspace_bytes, hytopk_stats* stats_out,
+                               const hytopk_select_options* opts, cudaStream_t stream) {
+  hytopk_status s = check_shape(n, L, H, d, k_top, dt);
+  if (s != HYTOPK_OK) return s;
+  s = check_inputs(q, q_scale, k, k_scale, w, dt, n);
+  if (s != HYTOPK_OK) return s;
+  const int C = default_capacity(k_top, capacity);
+  if (capacity < 0 || C < k_top) return HYTOPK_INVALID_ARG;
+  if (n > 0 && (!positions || !idx_out || !workspace)) return HYTOPK_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HYTOPK_MISALIGNED;
+  const SelectLayout lay = select_layout(n, L, H, d, C, dt);
+  if (workspace_bytes < lay.total) return HYTOPK_WORKSPACE_TOO_SMALL;
+  if (n == 0) {
+    if (stats_out) HYTOPK_TRY(cudaMemsetAsync(stats_out, 0, sizeof(hytopk_stats), stream));
+    return HYTOPK_OK;
+  }
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  SelectWs ws;
+  ws.perm = reinterpret_cast<int32_t*>(base + lay.perm);
+  ws.qpos = reinterpret_cast<int32_t*>(base + lay.qpos);
+  ws.wq = reinterpret_cast<float*>(base + lay.wq);
+  ws.qp = base + lay.qp;
+  ws.thr = reinterpret_cast<float*>(base + lay.thr);
+  ws.cnt = reinterpret_cast<int32_t*>(base + lay.cnt);
+  ws.cand = reinterpret_cast<uint64_t*>(base + lay.cand);
+  ws.failed_list = reinterpret_cast<int32_t*>(base + lay.flist);
+  ws.failed = base + lay.failed;
+  ws.counters = reinterpret_cast<uint32_t*>(base + lay.ctr);
+  ws.rowbuf = reinterpret_cast<float*>(base + lay.rowbuf);
+  ws.rowlist = reinterpret_cast<uint64_t*>(base + lay.rowlist);
+  ws.n_pad = pad_queries(n);
+  ws.C = C;
+  const Problem p = make_problem(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt);
+  const float* override_thr = opts ? opts->threshold_override : nullptr;
+  const int reverse = opts ? opts->reverse_schedule : 0;
+
+  if ((s = record(opts, HYTOPK_PHASE_PREP, stream)) != HYTOPK_OK) return s;
+  HYTOPK_TRY(cudaMemsetAsync(ws.counters, 0, kCtrCount * sizeof(uint32_t), stream));
+  HYTOPK_TRY(cudaMemsetAsync(ws.cnt, 0, (size_t)ws.n_pad * 4, stream));
+  HYTOPK_TRY(launch_prep(p, ws, stream));
+  if ((s = record(opts, HYTOPK_PHASE_THRESHOLD, stream)) != HYTOPK_OK) return s;
+  HYTOPK_TRY(launch_threshold(p, ws, override_thr, stream));
+  if ((s = record(opts, HYTOPK_PHASE_FILTER, stream)) != HYTOPK_OK) return s;
+  HYTOPK_TRY(launch_filter(p, ws, reverse, stream));
+  if ((s = record(opts, HYTOPK_PHASE_CHECK, stream)) != HYTOPK_OK) return s;
+  HYTOPK_TRY(launch_check(p, ws, stream));
+  if ((s = record(opts, HYTOPK_PHASE_SELECT, stream)) != HYTOPK_OK) return s;
+  HYTOPK_TRY(launch_select(p, ws, idx_out, scores_out, stream));
+  if ((s = record(opts, HYTOPK_PHASE_RECOVER, stream)) != HYTOPK_OK) return s;
+  HYTOPK_TRY(launch_recover(p, ws, idx_out, scores_out, stream));
+  if ((s = record(opts, HYTOPK_NUM_PHASES, stream)) != HYTOPK_OK) return s;
+  if (stats_out) HYTOPK_TRY(launch_finalize(ws, n, stats_out, stream));
+  return HYTOPK_OK;
+}
+
+hytopk_status hytopk_select(const void* q, const float* q_scale, const void* k,
+                            const float* k_scale, const float* w, const int32_t* positions, int n,
+                            int L, int H, int d, int k_top, hytopk_dtype dt, int32_t* idx_out,
+                            float* scores_out, int capacity, void* workspace,
+                            size_t workspace_bytes, hytopk_stats* stats_out, cudaStream_t stream) {
+  return hytopk_select_ex(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt, idx_out,
+                          scores_out, capacity, workspace, workspace_bytes, stats_out, nullptr,
+                          stream);
+}
+
+hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
+                            const float* k_scale, const float* w, const int32_t* idx, int n,
+                            int L, int H, int d, int k_top, hytopk_dtype dt, float* scores_out,
+                            uint32_t* dev_status, cudaStream_t stream) {
+  hytopk_status s = check_shape(n, L, H, d, k_top, dt);
+  if (s != HYTOPK_OK) return s;
+  s = check_inputs(q, q_scale, k, k_scale, w, dt, n);
+  if (s != HYTOPK_OK) return s;
+  if (n == 0) return HYTOPK_OK;
+  if (!idx || !scores_out) return HYTOPK_INVALID_ARG;
+  const Problem p = make_problem(q, q_scale, k, k_scale, w, nullptr, n, L, H, d, k_top, dt);
+  HYTOPK_TRY(launch_replay(p, idx, scores_out, dev_status, stream));
+  return HYTOPK_OK;
+}
+
+static size_t twopass_fixed_bytes(int L) {
+  return align_up((size_t)kRecoveryCtas * L * 8, 1024);
+}
+
+size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,
+                                     int rows_per_chunk) {
+  if (check_shape(n, L, H, d, k_top, dt) != HYTOPK_OK) return 0;
+  const int rows = rows_per_chunk <= 0 ? (n > 0 ? n : 1) : rows_per_chunk;
+  return twopass_fixed_bytes(L) + align_up((size_t)rows * L * 4, 1024);
+}
+
+hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const void* k,
+                                    const float* k_scale, const float* w,
+                                    const int32_t* positions, int n, int L, int H, int d,
+                                    int k_top, hytopk_dtype dt, int32_t* idx_out,
+                                    float* scores_out, void* workspace, size_t workspace_bytes,
+                                    uint32_t* dev_status, cudaStream_t stream) {
+  hytopk_status s = check_shape(n, L, H, d, k_top, dt);
+  if (s != HYTOPK_OK) return s;
+  s = check_inputs(q, q_scale, k, k_scale, w, dt, n);
+  if (s != HYTOPK_OK) return s;
+  if (n == 0) return HYTOPK_OK;
+  if (!positions || !idx_out || !workspace) return HYTOPK_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HYTOPK_MISALIGNED;
+  const size_t fixed = twopass_fixed_bytes(L);
+  const size_t row_bytes = (size_t)L * 4;
+  if (workspace_bytes < fixed + row_bytes) return HYTOPK_WORKSPACE_TOO_SMALL;
+  size_t chunk = (workspace_bytes - fixed) / row_bytes;
+  if (chunk > (size_t)n) chunk = (size_t)n;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  uint64_t* lists = reinterpret_cast<uint64_t*>(base);
+  float* table = reinterpret_cast<float*>(base + fixed);
+  const Problem p = make_problem(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt);
+  for (int row0 = 0; row0 < n; row0 += (int)chunk) {
+    const int rows = (int)((size_t)(n - row0) < chunk ? (size_t)(n - row0) : chunk);
+    HYTOPK_TRY(launch_table(p, row0, rows, table, dev_status, stream));
+    HYTOPK_TRY(launch_table_topk(p, row0, rows, table, lists, kRecoveryCtas, idx_out, scores_out,
+                                 stream));
+  }
+  return HYTOPK_OK;
+}
+
+const char* hytopk_status_string(hytopk_status status) {
+  switch (status) {
+    case HYTOPK_OK: return "ok";
+    case HYTOPK_INVALID_ARG: return "invalid argument";
+    case HYTOPK_UNSUPPORTED: return "unsupported shape or dtype";
+    case HYTOPK_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case HYTOPK_CUDA_ERROR: return "CUDA error";
+    case HYTOPK_MISALIGNED: return "device pointer not 16-byte aligned";
+  }
+  return "unknown status";
+}
+
+int hytopk_version(void) { return kVersion; }
+
+}  // extern "C"

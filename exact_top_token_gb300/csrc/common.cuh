@@ -1,0 +1,199 @@
+// common.cuh -- device-side definitions shared by the HyTopK kernels.
+//
+// Score arithmetic (identical in every kernel, so that the filter, the
+// recovery path, the two-pass path and replay return the same bits for the
+// same (query, key)):
+//
+//   dot_h  = sum_i q[t,h,i] * k[s,i]           raw elements (e4m3 codes or bf16)
+//   acc    = sum_h wq[t,h] * max(dot_h, 0)     h = 0..H-1, fused multiply-add
+//   score  = acc * k_scale[s]                  (k_scale = 1 for bf16)
+//
+// with wq[t,h] = w[t,h] * q_scale[t,h] (w for bf16). Because the scales are
+// positive, ReLU(qs*ks*x) = qs*ks*ReLU(x), so this equals the indexer score
+// I[t,s] = sum_h w[t,h] ReLU(q[t,h].k[s]) of the HyScale pages up to rounding.
+// -0.0 is returned as +0.0.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "hytopk.h"
+
+namespace hytopk {
+
+constexpr int kTileKeys = 128;       // keys per scoring tile (one TMEM lane / thread each)
+constexpr int kQueryPad = 128;       // query slots are padded to a multiple of this
+constexpr int kMaxSamples = 8192;    // upper clamp of the sample count M
+constexpr int kRecoveryCtas = 128;   // persistent CTAs of the recovery kernel
+constexpr int kMaxTopK = 16384;
+
+// Counters kept in the workspace (zeroed at the start of every call).
+enum Counter : int {
+  kCtrFilterWork = 0,
+  kCtrFailed = 1,
+  kCtrOverflow = 2,
+  kCtrUnderK = 3,
+  kCtrStatus = 4,
+  kCtrRecoverWork = 5,
+  kCtrCandLo = 6,  // 64-bit total candidates at [6,7]
+  kCtrCount = 16
+};
+
+struct Problem {
+  const void* q;
+  const float* q_scale;
+  const void* k;
+  const float* k_scale;
+  const float* w;
+  const int32_t* positions;
+  int n, L, H, d, k_top, dt;  // dt: 0 bf16, 1 e4m3
+};
+
+// Workspace of hytopk_select, carved by the host.
+struct SelectWs {
+  int32_t* perm;        // [n_pad] slot -> query index, -1 for padding
+  int32_t* qpos;        // [n_pad] slot -> position, -1 for padding / bad position
+  float* wq;            // [n_pad, H] folded head weights
+  void* qp;             // [n_pad, H, d] packed query elements
+  float* thr;           // [n_pad] thresholds
+  int32_t* cnt;         // [n_pad] candidate counts (may exceed C: overflow)
+  uint64_t* cand;       // [n_pad, C] candidate keys
+  int32_t* failed_list; // [n_pad]
+  uint8_t* failed;      // [n_pad]
+  uint32_t* counters;   // [kCtrCount]
+  float* rowbuf;        // [kRecoveryCtas, L] full score rows (recovery)
+  uint64_t* rowlist;    // [kRecoveryCtas, L] row candidate lists (recovery)
+  int n_pad, C;
+};
+
+// ---- element decoding --------------------------------------------------------
+
+__device__ __forceinline__ float bf16_value(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ float e4m3_value(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Load key row s (D elements) as floats, raw (no scale).
+template <int D, int DT>
+__device__ __forceinline__ void load_key_row(const void* kbase, size_t s, float (&kr)[D]) {
+  if (DT == 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(kbase) + s * D);
+#pragma unroll
+    for (int v = 0; v < D / 8; ++v) {
+      uint4 x = __ldg(src + v);
+      uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        kr[v * 8 + 2 * j] = __uint_as_float(wv[j] << 16);
+        kr[v * 8 + 2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
+      }
+    }
+  } else {
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(kbase) + s * D);
+#pragma unroll
+    for (int v = 0; v < D / 16; ++v) {
+      uint4 x = __ldg(src + v);
+      uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) kr[v * 16 + 4 * j + b] = e4m3_value((wv[j] >> (8 * b)) & 0xFF);
+    }
+  }
+}
+
+// Decode one (query, head) row of D raw elements into shared memory.
+template <int DT>
+__device__ __forceinline__ float load_elem(const void* base, size_t i) {
+  if (DT == 0) return bf16_value(reinterpret_cast<const uint16_t*>(base)[i]);
+  return e4m3_value(reinterpret_cast<const uint8_t*>(base)[i]);
+}
+
+// ---- the score ------------------------------------------------------------------
+
+__device__ __forceinline__ float finish_score(float acc, float ks) {
+  float s = acc * ks;
+  return s == 0.0f ? 0.0f : s;
+}
+
+// Score of one key (raw row in registers) for one query whose raw q rows
+// [H][D] and folded weights [H] sit in shared memory.
+template <int D>
+__device__ __forceinline__ float score_key_simt(const float* __restrict__ qf,
+                                                const float* __restrict__ wq, int H,
+                                                const float (&kr)[D], float ks) {
+  float acc = 0.0f;
+  for (int h = 0; h < H; ++h) {
+    const float4* q4 = reinterpret_cast<const float4*>(qf + h * D);
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) {
+      float4 v = q4[i];
+      dot = fmaf(v.x, kr[4 * i + 0], dot);
+      dot = fmaf(v.y, kr[4 * i + 1], dot);
+      dot = fmaf(v.z, kr[4 * i + 2], dot);
+      dot = fmaf(v.w, kr[4 * i + 3], dot);
+    }
+    acc = fmaf(wq[h], fmaxf(dot, 0.0f), acc);
+  }
+  return finish_score(acc, ks);
+}
+
+// ---- ordered keys -------------------------------------------------------------------
+// desc32(score): an unsigned key whose ascending order is descending score.
+// cand_key(score, pos) = desc32 << 32 | pos: ascending order is score
+// descending, then position ascending -- the output order of the selection.
+
+__device__ __forceinline__ uint32_t desc32(float f) {
+  uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+  uint32_t asc = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ~asc;
+}
+
+__device__ __forceinline__ float desc32_score(uint32_t k) {
+  uint32_t asc = ~k;
+  uint32_t u = (asc & 0x80000000u) ? (asc & 0x7FFFFFFFu) : ~asc;
+  return __uint_as_float(u);
+}
+
+__device__ __forceinline__ uint64_t cand_key(float score, int32_t pos) {
+  return ((uint64_t)desc32(score) << 32) | (uint32_t)pos;
+}
+
+// ---- threshold parameters (HyScale explainer: HyTopK paragraph, worked example) ----
+
+__device__ __forceinline__ int sample_count(int64_t ctx) {
+  int64_t m = ctx / 128;
+  m = m < 4096 ? 4096 : m;
+  m = m > kMaxSamples ? kMaxSamples : m;
+  return (int)(m < ctx ? m : ctx);
+}
+
+__device__ __forceinline__ int threshold_rank(int64_t ctx, int64_t k, int m) {
+  int64_t r = (3 * k * (int64_t)m + ctx - 1) / ctx;
+  return (int)(r < m ? r : m);
+}
+
+__device__ __forceinline__ int sample_position(int64_t ctx, int m, int j) {
+  return (int)(((int64_t)j * ctx) / m);
+}
+
+// Entries of the shared-memory sort buffer for k keys: the next power of two,
+// at least 2 (so that what follows it stays 16-byte aligned).
+__host__ __device__ __forceinline__ int sort_capacity(int k) {
+  int P = 2;
+  while (P < k) P <<= 1;
+  return P;
+}
+
+// ---- small CTA utilities ---------------------------------------------------------
+
+__device__ __forceinline__ void set_status(uint32_t* counters, uint32_t bits) {
+  atomicOr(counters + kCtrStatus, bits);
+}
+
+}  // namespace hytopk

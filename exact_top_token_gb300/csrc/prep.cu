@@ -1,0 +1,98 @@
+// prep.cu -- order the queries by position and pack them for the scoring
+// kernels.
+//
+// Queries are placed in "slots" sorted by position, longest context first,
+// so that a block of adjacent slots has nearly equal causal ranges (little
+// masked work in a shared key tile) and the longest blocks are scheduled
+// first. Packing copies each query's q rows to its slot, folds the fp8 query
+// scale into the head weight (wq = w * q_scale, valid because scales are
+// positive) and records the position. Slots past n are padding with
+// position -1 (no keys).
+#include <climits>
+
+#include "launch.h"
+
+namespace hytopk {
+
+namespace {
+
+__device__ __forceinline__ int clean_position(const int32_t* positions, int t, int L) {
+  const int p = positions[t];
+  return (p >= 0 && p < L) ? p : -1;
+}
+
+// slot(t) = #{u : pos(u) > pos(t) or (pos(u) == pos(t) and u < t)}: a stable
+// descending sort by rank counting.
+__global__ void __launch_bounds__(1024) k_rank_by_position(const int32_t* __restrict__ positions,
+                                                            int n, int L,
+                                                            int32_t* __restrict__ perm) {
+  __shared__ int tile[1024];
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int mine = t < n ? clean_position(positions, t, L) : INT_MIN;
+  int rank = 0;
+  for (int base = 0; base < n; base += 1024) {
+    const int u = base + threadIdx.x;
+    tile[threadIdx.x] = u < n ? clean_position(positions, u, L) : INT_MIN;
+    __syncthreads();
+    const int lim = min(1024, n - base);
+    for (int j = 0; j < lim; ++j) {
+      const int pu = tile[j];
+      rank += (pu > mine) | ((pu == mine) & (base + j < t));
+    }
+    __syncthreads();
+  }
+  if (t < n) perm[rank] = t;
+}
+
+__global__ void __launch_bounds__(128) k_pack_queries(Problem p, SelectWs ws) {
+  const int slot = blockIdx.x;
+  const int t = slot < p.n ? ws.perm[slot] : -1;
+  const int esize = p.dt == 0 ? 2 : 1;
+  const size_t row_bytes = (size_t)p.H * p.d * esize;  // multiple of 16
+  uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.qp) + slot * row_bytes);
+  const int nvec = (int)(row_bytes / 16);
+  if (t < 0) {
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+    for (int h = threadIdx.x; h < p.H; h += blockDim.x) ws.wq[(size_t)slot * p.H + h] = 0.0f;
+    if (threadIdx.x == 0) {
+      ws.qpos[slot] = -1;
+      ws.perm[slot] = -1;
+    }
+    return;
+  }
+  const uint4* src =
+      reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.q) + (size_t)t * row_bytes);
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = src[v];
+  for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
+    float wv = p.w[(size_t)t * p.H + h];
+    if (p.dt == 1) {
+      const float qs = p.q_scale[(size_t)t * p.H + h];
+      if (!(qs > 0.0f)) set_status(ws.counters, HYTOPK_DEV_BAD_SCALE);
+      wv *= qs;
+    }
+    ws.wq[(size_t)slot * p.H + h] = wv;
+  }
+  if (threadIdx.x == 0) {
+    const int pos = clean_position(p.positions, t, p.L);
+    if (pos < 0) set_status(ws.counters, HYTOPK_DEV_BAD_POSITION);
+    ws.qpos[slot] = pos;
+  }
+}
+
+__global__ void k_check_key_scales(const float* __restrict__ k_scale, int L, uint32_t* counters) {
+  bool bad = false;
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < L; s += gridDim.x * blockDim.x)
+    bad |= !(k_scale[s] > 0.0f);
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(counters, HYTOPK_DEV_BAD_SCALE);
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const Problem& p, const SelectWs& ws, cudaStream_t st) {
+  if (p.n > 0) k_rank_by_position<<<(p.n + 1023) / 1024, 1024, 0, st>>>(p.positions, p.n, p.L, ws.perm);
+  if (ws.n_pad > 0) k_pack_queries<<<ws.n_pad, 128, 0, st>>>(p, ws);
+  if (p.dt == 1) k_check_key_scales<<<64, 256, 0, st>>>(p.k_scale, p.L, ws.counters);
+  return cudaGetLastError();
+}
+
+}  // namespace hytopk

@@ -1,0 +1,209 @@
+// radix.cuh -- CTA-wide radix select and sort on ordered keys.
+//
+// The HyScale explainer (HyTopK paragraph) resolves ties at the k-th score
+// with a radix select over positions and orders the kept entries with a radix
+// sort, which makes the output independent of the order in which the
+// unordered atomic appends filled the candidate buffer. Here a candidate is
+// the 64-bit key desc32(score) << 32 | position: an MSB-first radix select
+// over its upper 32 bits is the select on score, and over its lower 32 bits
+// (reached only when scores tie at the boundary) the select over positions.
+// The k selected keys are unique, so the final order (ascending key = score
+// descending, position ascending) is a total order.
+#pragma once
+
+#include "common.cuh"
+
+namespace hytopk {
+
+// Block-wide: given hist[0..nbins), find the bin b where the running count
+// crosses `target` (1-based): sum(hist[<b]) < target <= sum(hist[<=b]).
+// Writes b and sum(hist[<b]) to out[0], out[1]. Needs blockDim.x % 32 == 0 and
+// a `warp_sums` array of blockDim.x/32 entries. All threads must call it.
+__device__ __forceinline__ void cta_find_crossing(const uint32_t* hist, int nbins, uint32_t target,
+                                                  uint32_t* warp_sums, uint32_t* out) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int per = (nbins + nthr - 1) / nthr;
+  const int b0 = tid * per;
+  uint32_t local = 0;
+  for (int b = b0; b < b0 + per && b < nbins; ++b) local += hist[b];
+  // inclusive warp scan
+  uint32_t incl = local;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  uint32_t before_warp = 0;
+  for (int w = 0; w < warp; ++w) before_warp += warp_sums[w];
+  const uint32_t excl = before_warp + incl - local;
+  if (excl < target && target <= excl + local) {
+    uint32_t cum = excl;
+    for (int b = b0; b < b0 + per && b < nbins; ++b) {
+      if (cum + hist[b] >= target) {
+        out[0] = (uint32_t)b;
+        out[1] = cum;
+        break;
+      }
+      cum += hist[b];
+    }
+  }
+  __syncthreads();
+}
+
+// Shared-memory scratch of the selection helpers.
+struct alignas(16) RadixScratch {
+  uint32_t hist[4096];
+  uint32_t warp_sums[32];
+  uint32_t out[4];
+  uint32_t counter;
+};
+
+// The kk-th smallest (1-based) of keys[0..cnt) (32-bit, duplicates allowed).
+static __device__ uint32_t cta_kth_smallest_u32(const uint32_t* keys, int cnt, uint32_t kk,
+                                         RadixScratch& sc) {
+  uint32_t prefix = 0;
+  for (int pbits = 0; pbits < 32; pbits += 8) {
+    const int shift = 24 - pbits;
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) sc.hist[b] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+      const uint32_t key = keys[e];
+      if (pbits == 0 || (key >> (32 - pbits)) == prefix) atomicAdd(&sc.hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    cta_find_crossing(sc.hist, 256, kk, sc.warp_sums, sc.out);
+    const uint32_t bin = sc.out[0], before = sc.out[1];
+    kk -= before;
+    prefix = (prefix << 8) | bin;
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Selects the k_sel smallest of the unique keys list[0..cnt) into sel[0..k_sel)
+// (shared memory, unordered). Returns the number written (min(cnt, k_sel)).
+static __device__ int cta_select_smallest_u64(const uint64_t* list, int cnt, int k_sel, uint64_t* sel,
+                                       RadixScratch& sc) {
+  if (cnt <= k_sel) {
+    for (int e = threadIdx.x; e < cnt; e += blockDim.x) sel[e] = list[e];
+    __syncthreads();
+    return cnt;
+  }
+  uint64_t prefix = 0;
+  int pbits = 0;
+  uint32_t krem = (uint32_t)k_sel;
+  while (pbits < 64) {
+    const int shift = 56 - pbits;
+    for (int b = threadIdx.x; b < 256; b += blockDim.x) sc.hist[b] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+      const uint64_t key = list[e];
+      if (pbits == 0 || (key >> (64 - pbits)) == prefix)
+        atomicAdd(&sc.hist[(uint32_t)(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    cta_find_crossing(sc.hist, 256, krem, sc.warp_sums, sc.out);
+    const uint32_t bin = sc.out[0], before = sc.out[1];
+    const bool whole_bin = (sc.hist[bin] == krem - before);
+    krem -= before;
+    prefix = (prefix << 8) | bin;
+    pbits += 8;
+    __syncthreads();
+    if (whole_bin) break;
+  }
+  if (threadIdx.x == 0) sc.counter = 0;
+  __syncthreads();
+  const int drop = 64 - pbits;
+  for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
+    const uint64_t key = list[e];
+    if ((drop == 64 ? 0ull : (key >> drop)) <= prefix) sel[atomicAdd(&sc.counter, 1u)] = key;
+  }
+  __syncthreads();
+  return k_sel;
+}
+
+// Ascending sort of sel[0..n) in shared memory; entries n..P-1 (P = next
+// power of two) are filled with ~0 and sort last.
+static __device__ void cta_sort_u64(uint64_t* sel, int n) {
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int e = n + threadIdx.x; e < P; e += blockDim.x) sel[e] = ~0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint64_t a = sel[lo], b = sel[hi];
+        if ((a > b) == up) {
+          sel[lo] = b;
+          sel[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Write one query's sorted selection: k_eff keys then padding to k_top.
+__device__ __forceinline__ void write_selection(const uint64_t* sel, int k_eff, int k_top,
+                                                int32_t* idx_row, float* score_row) {
+  for (int j = threadIdx.x; j < k_top; j += blockDim.x) {
+    if (j < k_eff) {
+      const uint64_t key = sel[j];
+      idx_row[j] = (int32_t)(uint32_t)key;
+      if (score_row) score_row[j] = desc32_score((uint32_t)(key >> 32));
+    } else {
+      idx_row[j] = -1;
+      if (score_row) score_row[j] = -__int_as_float(0x7f800000);
+    }
+  }
+}
+
+// Exact top-k of a full score row[0..ctx): a 12-bit histogram of desc32 finds
+// the bin holding the k-th best score, the keys in and above that bin are
+// listed (list: ctx entries of global scratch), and the list is radix
+// selected and sorted. Result: sel[0..min(k,ctx)) sorted.
+static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_t* list, uint64_t* sel,
+                            RadixScratch& sc) {
+  const int k_eff = ctx < k_top ? ctx : k_top;
+  if (k_eff <= 0) return 0;
+  for (int b = threadIdx.x; b < 4096; b += blockDim.x) sc.hist[b] = 0;
+  __syncthreads();
+  for (int s = threadIdx.x; s < ctx; s += blockDim.x) atomicAdd(&sc.hist[desc32(row[s]) >> 20], 1u);
+  __syncthreads();
+  cta_find_crossing(sc.hist, 4096, (uint32_t)k_eff, sc.warp_sums, sc.out);
+  const uint32_t bin = sc.out[0];
+  if (threadIdx.x == 0) sc.counter = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  for (int s0 = 0; s0 < ctx; s0 += blockDim.x) {
+    const int s = s0 + threadIdx.x;
+    float v = 0.0f;
+    bool take = false;
+    if (s < ctx) {
+      v = row[s];
+      take = (desc32(v) >> 20) <= bin;
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, take);
+    if (mask) {
+      const int leader = __ffs(mask) - 1;
+      uint32_t base = 0;
+      if (lane == leader) base = atomicAdd(&sc.counter, (uint32_t)__popc(mask));
+      base = __shfl_sync(0xffffffffu, base, leader);
+      if (take) list[base + __popc(mask & ((1u << lane) - 1u))] = cand_key(v, s);
+    }
+  }
+  __syncthreads();
+  const int listed = (int)sc.counter;
+  __syncthreads();
+  const int got = cta_select_smallest_u64(list, listed, k_eff, sel, sc);
+  cta_sort_u64(sel, got);
+  return got;
+}
+
+}  // namespace hytopk

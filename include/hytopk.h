@@ -1,0 +1,206 @@
+/*
+ * hytopk.h -- exact per-query top-k selection over DeepSeek-style indexer
+ * scores without a score table (HyTopK, also called FlashTopK), selection
+ * replay, and the conventional two-pass materialise-then-top-k path, for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and paragraph:
+ *   [Summary]   "HyScale: Scaling Long-Context Training for Learned Sparse
+ *               Attention" (neuraltrendhub), "What the paper found" and
+ *               "Original abstract".
+ *   [Explainer] "HyScale sparse-attention training -- Selection without a
+ *               score table -- What does it mean?" (learnaivisually): the
+ *               score-table, HyTopK, selection-replay and worked-example
+ *               paragraphs.
+ *
+ * The operation. For query t at position pos[t] (it sees keys s <= pos[t],
+ * "every earlier token", Summary) the indexer score is
+ *
+ *     I[t,s] = sum_h w[t,h] * ReLU( q[t,h,:] . k[s,:] )
+ *
+ * with one shared key head. hytopk_select returns, per query, the exact top-k
+ * key positions of I[t, 0..pos[t]] ordered by score descending, ties by lower
+ * position first (Explainer, HyTopK paragraph: ties at the k-th score are
+ * resolved by position and the k kept entries are radix sorted, so the output
+ * is bitwise reproducible), without writing the n x L score table to memory.
+ * hytopk_replay rescores only stored (query, index) pairs (Explainer,
+ * selection-replay paragraph). hytopk_select_twopass is the conventional
+ * method (Explainer, score-table paragraph): a kernel writes every score, a
+ * second kernel reads them back and selects.
+ *
+ * Conventions shared by every call:
+ *   - Every array pointer is DEVICE memory owned by the caller. The library
+ *     allocates nothing and keeps no state between calls; scratch memory is
+ *     the caller's `workspace`.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream). The
+ *     return code covers host-side argument checks and launch errors only;
+ *     conditions found on the device are reported through the device status
+ *     word (HYTOPK_DEV_* bits) of hytopk_stats or of the replay call.
+ *   - Layouts are row-major and contiguous:
+ *       q        [n, H, d] elements of `dt`
+ *       q_scale  [n, H]    fp32, one scale per (query, head) row of d elements;
+ *                          required for HYTOPK_E4M3, must be NULL for bf16
+ *       k        [L, d]    elements of `dt`
+ *       k_scale  [L]       fp32 per key row; required for e4m3, NULL for bf16
+ *       w        [n, H]    fp32 head weights (any sign)
+ *       positions[n]       int32, 0 <= pos < L, any order
+ *     e4m3 is OCP FP8 E4M3 ("fn"); an element's value is code * scale. Scales
+ *     must be finite and > 0 (then ReLU(a*x) = a*ReLU(x) and scales may be
+ *     applied after the dot); a non-positive scale sets HYTOPK_DEV_BAD_SCALE.
+ *     Inputs must be finite.
+ *   - Supported shapes: H in {1,2,4,8,16,32,64,128}, d in {64,128}, d*elem
+ *     size a multiple of 16 bytes; 1 <= k_top <= 16384; n >= 0; L >= 1.
+ *     Other shapes return HYTOPK_UNSUPPORTED.
+ *   - Device pointers must be 16-byte aligned.
+ *   - Scores are fp32. A selected score agrees with the definition above to
+ *     within 1e-3 relative (exact for integer-valued data that fits fp32).
+ */
+#ifndef HYTOPK_H
+#define HYTOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HYTOPK_OK = 0,
+  HYTOPK_INVALID_ARG = 1,          /* null pointer, negative size, bad enum, k_top > capacity */
+  HYTOPK_UNSUPPORTED = 2,          /* H, d or k_top outside the supported set */
+  HYTOPK_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the *_workspace_size value */
+  HYTOPK_CUDA_ERROR = 4,           /* a CUDA runtime call or launch failed */
+  HYTOPK_MISALIGNED = 5            /* a device pointer is not 16-byte aligned */
+} hytopk_status;
+
+typedef enum { HYTOPK_BF16 = 0, HYTOPK_E4M3 = 1 } hytopk_dtype;
+
+/* Device status bits (written with atomicOr on the device). */
+#define HYTOPK_DEV_REPLAY_BAD_INDEX 0x1u /* replay index not -1 and outside [0, L): entry is NaN */
+#define HYTOPK_DEV_BAD_SCALE 0x2u        /* a q_scale or k_scale <= 0 (results undefined) */
+#define HYTOPK_DEV_BAD_POSITION 0x4u     /* a position outside [0, L): that query is all -1 */
+
+/* Per-call statistics of hytopk_select (device memory, written at the end of
+ * the call's stream work). The check kernel flags a query with ctx > k whose
+ * candidate count is below k (under-k) or above the capacity (overflow)
+ * (Explainer, HyTopK paragraph); when more than 64 queries fail, every query
+ * is rescored over its whole context (fallback_used = 1). */
+typedef struct {
+  int32_t n_failed;
+  int32_t n_overflow;
+  int32_t n_under_k;
+  int32_t fallback_used;
+  int64_t total_candidates; /* sum over queries of the filter's candidate count */
+  uint32_t device_status;   /* HYTOPK_DEV_* bits */
+  int32_t n_queries;
+} hytopk_stats;
+
+/* Largest number of failed queries repaired one by one; above it the whole
+ * selection is rescored (Explainer, HyTopK paragraph: "more than 64"). */
+#define HYTOPK_MAX_RECOVERY_ROWS 64
+
+/* Phase boundaries of hytopk_select that hytopk_select_ex can time. */
+enum {
+  HYTOPK_PHASE_PREP = 0,      /* order queries by position, pack q, fold scales */
+  HYTOPK_PHASE_THRESHOLD = 1, /* score the evenly spaced samples, take the r-th best */
+  HYTOPK_PHASE_FILTER = 2,    /* score every causal key, keep those >= threshold */
+  HYTOPK_PHASE_CHECK = 3,     /* flag under-k and overflowed queries */
+  HYTOPK_PHASE_SELECT = 4,    /* exact radix select + sort of the candidates */
+  HYTOPK_PHASE_RECOVER = 5,   /* rescore failed queries over their whole context */
+  HYTOPK_NUM_PHASES = 6
+};
+
+/* Options of hytopk_select_ex. Zero-initialise for the defaults. */
+typedef struct {
+  /* Device fp32 [n] or NULL. Replaces the sampled threshold of each query
+   * (a testing hook: -inf forces overflow, +inf forces under-k). The result
+   * is the exact top-k whatever the thresholds are. */
+  const float* threshold_override;
+  /* NULL or HYTOPK_NUM_PHASES + 1 events recorded on `stream` before the
+   * first phase and after each phase (CUDA events, caller-created). */
+  cudaEvent_t* phase_events;
+  /* Nonzero: the filter walks its work list in reverse (determinism tests). */
+  int reverse_schedule;
+  int reserved;
+} hytopk_select_options;
+
+/* Bytes of workspace hytopk_select needs. capacity = candidate buffer slots
+ * per query (0 selects the default 8 * k_top). Returns 0 for invalid or
+ * unsupported arguments. */
+size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
+                                    hytopk_dtype dt);
+
+/* Exact top-k selection without a score table (HyTopK).
+ *   idx_out    [n, k_top] int32: key positions, score descending then position
+ *              ascending; a query with ctx = pos+1 < k_top has its ctx keys
+ *              followed by -1.
+ *   scores_out [n, k_top] fp32 or NULL: the scores of idx_out, -inf padding.
+ *   capacity   candidate slots per query, >= k_top (0: 8 * k_top).
+ *   workspace  device memory of at least hytopk_select_workspace_size(...)
+ *              bytes, 256-byte aligned; contents need not be initialised.
+ *   stats_out  device hytopk_stats or NULL.
+ * The steps: per query, M = min(ctx, max(4096, floor(ctx/128)), 8192) evenly
+ * spaced keys p_j = floor(j*ctx/M) are scored and the threshold T is the r-th
+ * best of them, r = min(M, ceil(3*k*M/ctx)) (Explainer, HyTopK paragraph and
+ * worked example); every causal key is scored on chip and keys with score >= T
+ * are appended to the query's candidate buffer; queries with ctx > k and fewer
+ * than k or more than `capacity` candidates are rescored over their whole
+ * context; the candidates are radix-selected (score, then position) and
+ * radix-sorted. */
+hytopk_status hytopk_select(const void* q, const float* q_scale, const void* k,
+                            const float* k_scale, const float* w, const int32_t* positions, int n,
+                            int L, int H, int d, int k_top, hytopk_dtype dt, int32_t* idx_out,
+                            float* scores_out, int capacity, void* workspace,
+                            size_t workspace_bytes, hytopk_stats* stats_out, cudaStream_t stream);
+
+/* hytopk_select with options (opts may be NULL). */
+hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* k,
+                               const float* k_scale, const float* w, const int32_t* positions,
+                               int n, int L, int H, int d, int k_top, hytopk_dtype dt,
+                               int32_t* idx_out, float* scores_out, int capacity,
+                               void* workspace, size_t workspace_bytes, hytopk_stats* stats_out,
+                               const hytopk_select_options* opts, cudaStream_t stream);
+
+/* Selection replay (Explainer, selection-replay paragraph): scores_out[t,j] =
+ * I[t, idx[t,j]] for idx [n, k_top] int32, with the same arithmetic as
+ * hytopk_select (so replayed scores equal the selected scores bit for bit).
+ * idx = -1 gives -inf. Any other index outside [0, L) gives NaN and sets
+ * HYTOPK_DEV_REPLAY_BAD_INDEX in *dev_status (device uint32, may be NULL).
+ * Replay does not check causality. Needs no workspace. */
+hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
+                            const float* k_scale, const float* w, const int32_t* idx, int n,
+                            int L, int H, int d, int k_top, hytopk_dtype dt, float* scores_out,
+                            uint32_t* dev_status, cudaStream_t stream);
+
+/* Bytes of workspace the two-pass path needs to hold `rows_per_chunk` rows of
+ * the score table at once (rows_per_chunk <= 0: all n rows). */
+size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,
+                                     int rows_per_chunk);
+
+/* The conventional two-pass path (Explainer, score-table paragraph): for each
+ * chunk of queries, one kernel writes the fp32 score rows [chunk, L] (-inf
+ * beyond each query's position) to the workspace and a second kernel reads
+ * them back and selects the exact top-k with the same tie rule and order as
+ * hytopk_select. The chunk size is the largest the workspace holds. Same
+ * outputs as hytopk_select. */
+hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const void* k,
+                                    const float* k_scale, const float* w,
+                                    const int32_t* positions, int n, int L, int H, int d,
+                                    int k_top, hytopk_dtype dt, int32_t* idx_out,
+                                    float* scores_out, void* workspace, size_t workspace_bytes,
+                                    uint32_t* dev_status, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* hytopk_status_string(hytopk_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int hytopk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYTOPK_H */

@@ -233,3 +233,21 @@ WORKLOADS = {
     "glm_1m": {"L": 1 << 20, "n": 8192, "H": 64, "d": 128, "k_top": 2048, "dtype": "e4m3"},
     "recovery_stress": {"L": 262144, "n": 2048, "H": 16, "d": 64, "k_top": 2048, "dtype": "bf16"},
 }
+
+
+def to_torch(case, device="cuda"):
+    """The case's arrays as torch tensors on `device` (bf16 / float8_e4m3fn
+    element types), in the layouts the library takes."""
+    import torch
+
+    def t(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+    if case["dtype"] == "bf16":
+        q = t(case["q"].view(np.int16)).view(torch.bfloat16)
+        k = t(case["k"].view(np.int16)).view(torch.bfloat16)
+    else:
+        q = t(case["q"]).view(torch.float8_e4m3fn)
+        k = t(case["k"]).view(torch.float8_e4m3fn)
+    return {"q": q, "k": k, "q_scale": t(case["q_scale"]), "k_scale": t(case["k_scale"]),
+            "w": t(case["w"]), "positions": t(case["positions"]), "k_top": case["k_top"]}

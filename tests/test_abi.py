@@ -1,0 +1,82 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+that include/hytopk.h declares, and its host-side argument checks return the
+documented status codes before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_top_token_gb300 as hk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hk.build()
+    return hk.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "hytopk.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hytopk_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(hk.symbols)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for code, text in hk.STATUS.items():
+        assert lib.hytopk_status_string(code).decode() == text
+    assert lib.hytopk_version() >= 100
+
+
+def test_workspace_size_rules(lib):
+    ws = lib.hytopk_select_workspace_size
+    assert ws(64, 4096, 4, 64, 256, 0, 0) > 0
+    assert ws(64, 4096, 4, 64, 256, 100, 0) == 0  # capacity below k
+    assert ws(64, 4096, 3, 64, 256, 0, 0) == 0  # H not a power of two
+    assert ws(64, 4096, 4, 96, 256, 0, 0) == 0  # d unsupported
+    assert ws(64, 4096, 4, 64, 0, 0, 0) == 0
+    assert ws(64, 4096, 4, 64, 256, 0, 7) == 0  # bad dtype
+    # candidate buffer dominates at the 1M setting: 8192 x 8k x 8 bytes
+    big = ws(8192, 1 << 20, 64, 128, 2048, 0, 1)
+    assert big >= 8192 * 16384 * 8
+    assert lib.hytopk_twopass_workspace_size(8192, 1 << 20, 64, 128, 2048, 1, 0) >= 32 * 2**30
+
+
+def test_host_checks_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every case fails a host check first
+    args = dict(q=fake, qs=None, k=fake, ks=None, w=fake, pos=fake, n=4, L=100, H=4, d=64,
+                k_top=8, dt=0, idx=fake, sc=None, cap=0, ws=fake, wsb=1 << 30, st=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.hytopk_select(a["q"], a["qs"], a["k"], a["ks"], a["w"], a["pos"], a["n"], a["L"],
+                                 a["H"], a["d"], a["k_top"], a["dt"], a["idx"], a["sc"], a["cap"],
+                                 a["ws"], a["wsb"], a["st"], None)
+
+    assert call(k=None) == 1
+    assert call(n=-1) == 1
+    assert call(H=6) == 2
+    assert call(d=32) == 2
+    assert call(k_top=20000) == 2
+    assert call(dt=1) == 1  # e4m3 needs scales
+    assert call(qs=fake) == 1  # bf16 takes no scales
+    assert call(cap=4) == 1  # capacity < k
+    assert call(wsb=16) == 3
+    assert call(q=P((1 << 20) + 4)) == 5
+    assert call(ws=P((1 << 20) + 128)) == 5
+    r = lib.hytopk_replay(fake, None, fake, None, fake, None, 4, 100, 4, 64, 8, 0, fake, None, None)
+    assert r == 1  # idx missing
+    assert lib.hytopk_select_twopass(fake, None, fake, None, fake, fake, 4, 100, 4, 64, 8, 0, fake,
+                                     None, fake, 16, None, None) == 3

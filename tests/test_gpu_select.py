@@ -1,0 +1,269 @@
+"""GPU parity: hytopk_select, hytopk_replay and the two-pass path against the
+CPU oracle, through the C ABI, on the named workloads and edge cases."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic_inputs as si
+from parity import check_structure, compare, run_select
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hk():
+    import exact_top_token_gb300 as hk
+
+    hk.build()
+    hk.load()
+    return hk
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import torch
+
+    return torch.device("cuda", 0)
+
+
+def host(*ts):
+    return [None if t is None else t.cpu().numpy() for t in ts]
+
+
+# ---- exact (integer-valued) workloads --------------------------------------------
+
+def test_tiny_exact_bit_exact(hk, dev):
+    case = si.tiny_exact()
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(64), gi, gs, exact=True)
+    stats = hk.read_stats(st)
+    fs = oracle.filter_sim(case, capacity=8 * 256)
+    assert stats["n_failed"] == int(fs["failed"].sum()) == 0
+    assert stats["total_candidates"] == int(fs["cnt"].sum())
+    assert stats["device_status"] == 0 and stats["n_queries"] == 64
+
+
+def test_recovery_small_per_row_recovery(hk, dev):
+    case = si.recovery_small(oracle.sample_positions)
+    C = 8 * case["k_top"]
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(len(case["positions"])), gi, gs, exact=True)
+    stats = hk.read_stats(st)
+    fs = oracle.filter_sim(case, capacity=C)
+    assert stats["n_failed"] == int(fs["failed"].sum()) > 0
+    assert stats["n_overflow"] == int((fs["cnt"] > C).sum())
+    assert stats["n_under_k"] == int((fs["cnt"] < case["k_top"]).sum())
+    assert stats["fallback_used"] == 0
+    assert stats["total_candidates"] == int(fs["cnt"].sum())
+
+
+@pytest.mark.slow
+def test_recovery_stress_full_fallback(hk, dev):
+    case = si.recovery_stress(oracle.sample_positions)
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    rows = si.sampled_rows(len(case["positions"]), 64)
+    rows = np.union1d(rows, case["decoy_rows"])
+    compare(case, rows, gi[rows], gs[rows], exact=True)
+    check_structure(gi, gs, case["positions"], case["k_top"])
+    stats = hk.read_stats(st)
+    assert stats["fallback_used"] == 1 and stats["n_failed"] > 64
+    fs = oracle.filter_sim(case, capacity=8 * case["k_top"], rows=rows)
+    flagged = set(rows[fs["failed"]].tolist())
+    assert flagged >= set(case["decoy_rows"].tolist())
+
+
+# ---- random workloads ---------------------------------------------------------------
+
+@pytest.mark.parametrize("L,n,H,d,k_top,dt,pos", [
+    (5000, 100, 32, 128, 300, "bf16", "random"),
+    (20000, 70, 64, 128, 512, "e4m3", "random"),
+    (9001, 33, 16, 64, 256, "bf16", "last"),
+    (3000, 129, 4, 64, 100, "e4m3", "spaced"),
+    (700, 5, 128, 128, 64, "bf16", "random"),
+    (4500, 40, 8, 64, 1, "bf16", "random"),
+    (130, 7, 2, 128, 200, "e4m3", "random"),
+])
+def test_random_small(hk, dev, L, n, H, d, k_top, dt, pos):
+    case = si.random_case(L, n, H, d, k_top, dt, seed=L + n, positions=pos)
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(n), gi, gs)
+    assert hk.read_stats(st)["device_status"] == 0
+
+
+@pytest.mark.slow
+def test_mixed_contexts_full(hk, dev):
+    case = si.mixed_contexts()
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(len(case["positions"])), gi, gs)
+    assert int((case["positions"] + 1 <= case["k_top"]).sum()) > 0  # some select-all rows
+
+
+@pytest.mark.slow
+def test_glm_1m_sampled_rows(hk, dev):
+    case = si.glm_1m()
+    idx, sc, st, t = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    rows = si.sampled_rows(len(case["positions"]), 48)
+    compare(case, rows, gi[rows], gs[rows])
+    check_structure(gi, gs, case["positions"], case["k_top"])
+    stats = hk.read_stats(st)
+    assert stats["device_status"] == 0
+    # replay of the forward indices on the same shapes
+    rs = hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"])
+    r_host = rs.cpu().numpy()
+    assert np.array_equal(r_host, gs)  # the same arithmetic as the selection
+    ref, bad = oracle.replay(si.subset(case, rows), gi[rows])
+    assert bad == 0
+    assert np.all(np.abs(r_host[rows] - ref) <= 1e-3 * np.maximum(np.abs(ref), 1e-30) +
+                  1e-3 * np.abs(ref).max(axis=1, keepdims=True))
+
+
+# ---- the threshold does not change the result (metamorphic) -----------------------------
+
+@pytest.mark.parametrize("mode", ["neg_inf", "pos_inf", "random"])
+def test_threshold_override_same_result(hk, dev, mode):
+    import torch
+
+    case = si.random_case(6000, 90, 16, 64, 128, "bf16", seed=21, positions="random",
+                          kind="int")
+    base, bsc, _, t = run_select(hk, case, dev)
+    n = len(case["positions"])
+    if mode == "neg_inf":
+        thr = torch.full((n,), -float("inf"), device=dev)
+    elif mode == "pos_inf":
+        thr = torch.full((n,), float("inf"), device=dev)
+    else:
+        thr = torch.from_numpy(np.random.Generator(np.random.PCG64(3)).uniform(
+            0, 80, n).astype(np.float32)).to(dev)
+    idx, sc, st, _ = run_select(hk, case, dev, threshold_override=thr, stats=True, capacity=300)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(n), gi, gs, exact=True)
+    stats = hk.read_stats(st)
+    ctx = case["positions"] + 1
+    expect = {"neg_inf": int((ctx > 300).sum()), "pos_inf": int((ctx > 128).sum())}
+    if mode in expect:
+        assert stats["n_failed"] == expect[mode]
+        assert stats["fallback_used"] == (expect[mode] > 64)
+
+
+def test_determinism_and_reverse_schedule(hk, dev):
+    case = si.random_case(12000, 64, 32, 128, 512, "e4m3", seed=22, positions="random")
+    runs = [run_select(hk, case, dev, reverse_schedule=(i % 2 == 1)) for i in range(4)]
+    first = host(runs[0][0], runs[0][1])
+    for r in runs[1:]:
+        other = host(r[0], r[1])
+        assert np.array_equal(first[0], other[0]) and np.array_equal(first[1], other[1])
+
+
+def test_power_of_two_weight_scaling(hk, dev):
+    case = si.random_case(3000, 20, 16, 64, 100, "bf16", seed=23, positions="random")
+    idx, sc, _, _ = run_select(hk, case, dev)
+    scaled = dict(case, w=case["w"] * np.float32(8.0))
+    idx2, sc2, _, _ = run_select(hk, scaled, dev)
+    gi, gs = host(idx, sc)
+    gi2, gs2 = host(idx2, sc2)
+    assert np.array_equal(gi, gi2)
+    valid = gi >= 0
+    assert np.array_equal(gs2[valid], gs[valid] * np.float32(8.0))
+
+
+def test_all_equal_scores_and_edge_rows(hk, dev):
+    import torch
+
+    n, L, H, d, k_top = 6, 300, 4, 64, 50
+    case = {"q": si.f32_to_bf16_bits(np.ones((n, H, d), np.float32)), "q_scale": None,
+            "k": si.f32_to_bf16_bits(np.ones((L, d), np.float32)), "k_scale": None,
+            "w": np.ones((n, H), np.float32),
+            "positions": np.array([299, 49, 0, 120, 10, 200], np.int32), "k_top": k_top,
+            "dtype": "bf16", "name": "equal"}
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(n), gi, gs, exact=True)
+    assert list(gi[0]) == list(range(50))
+    assert list(gi[2]) == [0] + [-1] * 49
+    # positions outside [0, L) give an all -1 row and the status bit
+    bad = dict(case, positions=np.array([299, -3, 300, 5, 1000, 7], np.int32))
+    idx, sc, st, _ = run_select(hk, bad, dev, stats=True)
+    gi, gs = host(idx, sc)
+    for r in (1, 2, 4):
+        assert np.all(gi[r] == -1) and np.all(np.isneginf(gs[r]))
+    assert list(gi[0]) == list(range(50)) and list(gi[3]) == list(range(6)) + [-1] * 44
+    assert hk.read_stats(st)["device_status"] & hk.DEV_BAD_POSITION
+    # an empty problem is a no-op
+    t = si.to_torch(case, dev)
+    e_idx, _, e_st = hk.select(t["q"][:0], t["k"], t["w"][:0], t["positions"][:0], k_top,
+                               stats=True)
+    assert e_idx.shape == (0, k_top) and hk.read_stats(e_st)["n_queries"] == 0
+
+
+# ---- replay ---------------------------------------------------------------------------
+
+def test_replay_parity_and_bad_indices(hk, dev):
+    import torch
+
+    case = si.random_case(8000, 50, 64, 128, 256, "e4m3", seed=24, positions="random")
+    idx, sc, _, t = run_select(hk, case, dev)
+    rs = hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"])
+    gi, gs, gr = host(idx, sc, rs)
+    assert np.array_equal(gr, gs)
+    ref, bad = oracle.replay(case, gi)
+    assert bad == 0
+    ok = gi >= 0
+    assert np.all(np.isneginf(gr[~ok]))
+    s_k = np.abs(ref).max(axis=1, keepdims=True)
+    assert np.all(np.abs(gr[ok] - ref[ok]) <= 1e-3 * np.broadcast_to(s_k, ref.shape)[ok])
+    idx2 = idx.clone()
+    idx2[0, 0] = 8000
+    idx2[3, 5] = -7
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rs2 = hk.replay(t["q"], t["k"], t["w"], idx2, q_scale=t["q_scale"], k_scale=t["k_scale"],
+                    status=status)
+    r2 = rs2.cpu().numpy()
+    assert np.isnan(r2[0, 0]) and np.isnan(r2[3, 5])
+    assert int(status.item()) & hk.DEV_REPLAY_BAD_INDEX
+
+
+def test_replay_random_indices_vs_oracle(hk, dev):
+    import torch
+
+    case = si.random_case(4000, 37, 16, 64, 333, "bf16", seed=25, positions="last")
+    g = np.random.Generator(np.random.PCG64(26))
+    idx = g.integers(-1, 4000, size=(37, 333)).astype(np.int32)
+    t = si.to_torch(case, dev)
+    rs = hk.replay(t["q"], t["k"], t["w"], torch.from_numpy(idx).to(dev))
+    ref, bad = oracle.replay(case, idx)
+    got = rs.cpu().numpy()
+    assert bad == 0
+    assert np.array_equal(np.isneginf(got), idx == -1)
+    ok = idx >= 0
+    scale = np.abs(ref[ok]).max()
+    assert np.all(np.abs(got[ok] - ref[ok]) <= 1e-3 * np.maximum(np.abs(ref[ok]), 1e-3 * scale))
+
+
+# ---- two-pass comparison path ------------------------------------------------------------
+
+@pytest.mark.parametrize("chunk", [0, 7])
+def test_twopass_matches_select(hk, dev, chunk):
+    case = si.random_case(7000, 45, 32, 128, 400, "bf16", seed=27, positions="random")
+    idx, sc, _, t = run_select(hk, case, dev)
+    ws = None
+    if chunk:
+        import torch
+
+        nbytes = hk.twopass_workspace_size(45, 7000, 32, 128, 400, hk.BF16, chunk)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], 400, workspace=ws)
+    assert np.array_equal(i2.cpu().numpy(), idx.cpu().numpy())
+    assert np.array_equal(s2.cpu().numpy(), sc.cpu().numpy())
+
+
+def test_twopass_exact_on_integer_data(hk, dev):
+    case = si.tiny_exact()
+    t = si.to_torch(case, dev)
+    i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], case["k_top"])
+    compare(case, np.arange(64), i2.cpu().numpy(), s2.cpu().numpy(), exact=True)
