@@ -252,7 +252,9 @@ def select_twopass(q, k, w, positions, k_top, *, q_scale=None, k_scale=None, row
     _check_tensor("positions", positions, dev, torch.int32, (n,))
     idx = torch.empty((n, k_top), dtype=torch.int32, device=dev)
     sc = torch.empty((n, k_top), dtype=torch.float32, device=dev) if scores else None
-    need = lib.hytopk_twopass_workspace_size(n, L, H, d, k_top, dt, rows_per_chunk)
+    # with a caller workspace the library picks the largest chunk that fits
+    need = lib.hytopk_twopass_workspace_size(n, L, H, d, k_top, dt,
+                                             1 if workspace is not None else rows_per_chunk)
     if need == 0:
         raise HytopkError(2, "hytopk_twopass_workspace_size")
     ws = _workspace(need, dev, workspace)

@@ -23,6 +23,10 @@ __device__ __forceinline__ void cta_find_crossing(const uint32_t* hist, int nbin
                                                   uint32_t* warp_sums, uint32_t* out) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int per = (nbins + nthr - 1) / nthr;
+  if (tid == 0) {
+    out[0] = 0;
+    out[1] = 0;
+  }
   const int b0 = tid * per;
   uint32_t local = 0;
   for (int b = b0; b < b0 + per && b < nbins; ++b) local += hist[b];
@@ -119,7 +123,10 @@ static __device__ int cta_select_smallest_u64(const uint64_t* list, int cnt, int
   const int drop = 64 - pbits;
   for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
     const uint64_t key = list[e];
-    if ((drop == 64 ? 0ull : (key >> drop)) <= prefix) sel[atomicAdd(&sc.counter, 1u)] = key;
+    if ((drop == 64 ? 0ull : (key >> drop)) <= prefix) {
+      const uint32_t at = atomicAdd(&sc.counter, 1u);
+      if (at < (uint32_t)k_sel) sel[at] = key;
+    }
   }
   __syncthreads();
   return k_sel;
