@@ -246,6 +246,12 @@ def gpu_arm(args, world, rank, local):
     nph = len(hk.PHASES) + 1
     step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
                    for _ in range(args.steps)]
+    # torch creates CUDA events lazily: record each once so that the handles
+    # exist before the library records them on the stream
+    for evs in step_events:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
 
     def step(events=None):
         hk.select(t["q"], t["k"], t["w"], t["positions"], k_top, q_scale=t["q_scale"],
