@@ -46,7 +46,7 @@ hytopk_status check_inputs(const void* q, const float* q_scale, const void* k, c
 int pad_queries(int n) { return (n + kQueryPad - 1) / kQueryPad * kQueryPad; }
 
 struct SelectLayout {
-  size_t perm, qpos, wq, qp, thr, cnt, cand, flist, failed, ctr, rowbuf, rowlist, total;
+  size_t perm, qpos, wq, qp, thr, cnt, cand, flist, failed, ctr, rowbuf, rowlist, plan, total;
 };
 
 SelectLayout select_layout(int n, int L, int H, int d, int C, hytopk_dtype dt) {
@@ -70,6 +70,7 @@ SelectLayout select_layout(int n, int L, int H, int d, int C, hytopk_dtype dt) {
   s.cand = take(np * (size_t)C * 8);
   s.rowbuf = take((size_t)kRecoveryCtas * L * 4);
   s.rowlist = take((size_t)kRecoveryCtas * L * 8);
+  s.plan = take(((size_t)stream_chunks(L) + 1) * 4);
   s.total = off;
   return s;
 }
@@ -153,6 +154,7 @@ hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* 
   ws.counters = reinterpret_cast<uint32_t*>(base + lay.ctr);
   ws.rowbuf = reinterpret_cast<float*>(base + lay.rowbuf);
   ws.rowlist = reinterpret_cast<uint64_t*>(base + lay.rowlist);
+  ws.plan = reinterpret_cast<int32_t*>(base + lay.plan);
   ws.n_pad = pad_queries(n);
   ws.C = C;
   const Problem p = make_problem(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt);

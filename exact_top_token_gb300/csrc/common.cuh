@@ -24,7 +24,7 @@
 namespace hytopk {
 
 constexpr int kTileKeys = 128;       // keys per scoring tile (one TMEM lane / thread each)
-constexpr int kQueryPad = 128;       // query slots are padded to a multiple of this
+constexpr int kQueryPad = 512;       // query slots are padded to a multiple of this
 constexpr int kMaxSamples = 8192;    // upper clamp of the sample count M
 constexpr int kRecoveryCtas = 128;   // persistent CTAs of the recovery kernel
 constexpr int kMaxTopK = 16384;
@@ -65,6 +65,7 @@ struct SelectWs {
   uint32_t* counters;   // [kCtrCount]
   float* rowbuf;        // [kRecoveryCtas, L] full score rows (recovery)
   uint64_t* rowlist;    // [kRecoveryCtas, L] row candidate lists (recovery)
+  int32_t* plan;        // [nchunks + 1] filter work items per key chunk
   int n_pad, C;
 };
 

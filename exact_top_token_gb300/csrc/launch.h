@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace hytopk {
@@ -29,6 +31,13 @@ cudaError_t launch_finalize(const SelectWs& ws, int n, hytopk_stats* stats, cuda
 cudaError_t launch_table_topk(const Problem& p, int row0, int rows, const float* table,
                               uint64_t* lists, int n_lists, int32_t* idx_out, float* scores_out,
                               cudaStream_t st);
+
+// tmap.cu
+bool make_tmap_2d(CUtensorMap* map, const void* base, int dt, uint64_t inner_elems, uint64_t rows,
+                  uint32_t box_inner_elems, uint32_t box_rows, int swizzle_bytes);
+int num_sms();
+int stream_chunks(int L);
+cudaError_t launch_plan(const SelectWs& ws, int L, int qb, cudaStream_t st);
 
 // Shared-memory bytes of the candidate selection for k_top.
 size_t select_smem_bytes(int k_top);

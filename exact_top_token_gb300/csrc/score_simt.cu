@@ -1,5 +1,5 @@
 // score_simt.cu -- scoring phases on the CUDA cores: sampled threshold,
-// fused score + filter, recovery rescoring, replay and the two-pass table.
+// recovery rescoring and replay.
 //
 // Every kernel evaluates the same per-(query, key) arithmetic
 // (score_key_simt in common.cuh): raw-element dots in fp32 with fused
@@ -12,8 +12,6 @@
 namespace hytopk {
 
 namespace {
-
-constexpr int kFilterQueries = 8;  // query slots per filter CTA
 
 // Decode the packed query rows of one slot (raw, [H][D]) and its folded
 // weights into shared memory.
@@ -63,55 +61,6 @@ __global__ void __launch_bounds__(256) k_threshold_simt(Problem p, SelectWs ws,
   __syncthreads();
   const uint32_t v = cta_kth_smallest_u32(keys, M, (uint32_t)r, sc);
   if (threadIdx.x == 0) ws.thr[slot] = desc32_score(v);
-}
-
-// ---- fused score + filter ---------------------------------------------------------
-__device__ __forceinline__ void append_candidate(bool pass, float sc, int s, int slot,
-                                                 int32_t* cnt, uint64_t* cand, int C) {
-  const unsigned mask = __ballot_sync(0xffffffffu, pass);
-  if (!mask) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(mask) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(cnt + slot, __popc(mask));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (pass) {
-    const int at = base + __popc(mask & ((1u << lane) - 1u));
-    if (at < C) cand[(size_t)slot * C + at] = cand_key(sc, s);
-  }
-}
-
-// grid.x: key tiles of 128, grid.y: groups of kFilterQueries slots.
-template <int D, int DT>
-__global__ void __launch_bounds__(128) k_filter_simt(Problem p, SelectWs ws, int reverse) {
-  extern __shared__ __align__(16) float fsm[];
-  float* qf = fsm;
-  float* wsm = qf + p.H * D;
-  const int tile = reverse ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
-  const int s0 = tile * kTileKeys;
-  const int s = s0 + threadIdx.x;
-  const int slot0 = blockIdx.y * kFilterQueries;
-  if (ws.qpos[slot0] < s0) return;  // slots are sorted by position, descending
-  float kr[D];
-  float ks = 0.0f;
-  if (s < p.L) {
-    load_key_row<D, DT>(p.k, (size_t)s, kr);
-    ks = key_scale(p, s);
-  } else {
-#pragma unroll
-    for (int i = 0; i < D; ++i) kr[i] = 0.0f;
-  }
-  for (int j = 0; j < kFilterQueries; ++j) {
-    const int slot = slot0 + j;
-    const int pos = ws.qpos[slot];
-    if (pos < s0) break;
-    __syncthreads();
-    load_query<D, DT>(ws.qp, (size_t)slot * p.H, p.H, ws.wq + (size_t)slot * p.H, qf, wsm);
-    __syncthreads();
-    const bool visible = s <= pos;
-    const float v = visible ? score_key_simt<D>(qf, wsm, p.H, kr, ks) : 0.0f;
-    append_candidate(visible && v >= ws.thr[slot], v, s, slot, ws.cnt, ws.cand, ws.C);
-  }
 }
 
 // ---- recovery -------------------------------------------------------------------------
@@ -196,47 +145,6 @@ __global__ void __launch_bounds__(128) k_replay_simt(Problem p, const int32_t* _
   if (bad && status) atomicOr(status, HYTOPK_DEV_REPLAY_BAD_INDEX);
 }
 
-// ---- two-pass table -----------------------------------------------------------------------
-// grid.x: key tiles, grid.y: groups of kFilterQueries rows. Writes every
-// score of rows [row0, row0+rows) to table[r, s]; -inf past each position.
-template <int D, int DT>
-__global__ void __launch_bounds__(128) k_table_simt(Problem p, int row0, int rows,
-                                                    float* __restrict__ table) {
-  extern __shared__ __align__(16) float tsm[];
-  float* qf = tsm;
-  float* wsm = qf + p.H * D;
-  const int s = blockIdx.x * kTileKeys + threadIdx.x;
-  float kr[D];
-  float ks = 0.0f;
-  if (s < p.L) {
-    load_key_row<D, DT>(p.k, (size_t)s, kr);
-    ks = key_scale(p, s);
-  } else {
-#pragma unroll
-    for (int i = 0; i < D; ++i) kr[i] = 0.0f;
-  }
-  for (int j = 0; j < kFilterQueries; ++j) {
-    const int r = blockIdx.y * kFilterQueries + j;
-    if (r >= rows) break;
-    const int t = row0 + r;
-    __syncthreads();
-    for (int i = threadIdx.x; i < p.H * D; i += blockDim.x)
-      qf[i] = load_elem<DT>(p.q, (size_t)t * p.H * D + i);
-    for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
-      float wv = p.w[(size_t)t * p.H + h];
-      if (p.dt == 1) wv *= p.q_scale[(size_t)t * p.H + h];
-      wsm[h] = wv;
-    }
-    __syncthreads();
-    const int pos = p.positions[t];
-    if (s < p.L) {
-      const float v = (s <= pos) ? score_key_simt<D>(qf, wsm, p.H, kr, ks)
-                                 : -__int_as_float(0x7f800000);
-      table[(size_t)r * p.L + s] = v;
-    }
-  }
-}
-
 #define HYTOPK_DISPATCH(D_, DT_, CALL)                 \
   do {                                                 \
     if ((D_) == 64 && (DT_) == 0) { CALL(64, 0); }     \
@@ -260,20 +168,6 @@ cudaError_t launch_threshold(const Problem& p, const SelectWs& ws, const float* 
 #define CALL(D, DT)                                                             \
   e = set_smem(k_threshold_simt<D, DT>, smem);                                  \
   if (e == cudaSuccess) k_threshold_simt<D, DT><<<ws.n_pad, 256, smem, st>>>(p, ws, override_thr);
-  HYTOPK_DISPATCH(p.d, p.dt, CALL);
-#undef CALL
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-cudaError_t launch_filter(const Problem& p, const SelectWs& ws, int reverse, cudaStream_t st) {
-  if (ws.n_pad == 0) return cudaSuccess;
-  const size_t smem = ((size_t)p.H * p.d + p.H) * 4;
-  const dim3 grid((p.L + kTileKeys - 1) / kTileKeys, ws.n_pad / kFilterQueries);
-  cudaError_t e = cudaSuccess;
-#define CALL(D, DT)                                       \
-  e = set_smem(k_filter_simt<D, DT>, smem);               \
-  if (e == cudaSuccess) k_filter_simt<D, DT><<<grid, 128, smem, st>>>(p, ws, reverse);
   HYTOPK_DISPATCH(p.d, p.dt, CALL);
 #undef CALL
   if (e != cudaSuccess) return e;
@@ -304,22 +198,6 @@ cudaError_t launch_replay(const Problem& p, const int32_t* idx, float* out, uint
 #define CALL(D, DT)                                    \
   e = set_smem(k_replay_simt<D, DT>, smem);            \
   if (e == cudaSuccess) k_replay_simt<D, DT><<<p.n, 128, smem, st>>>(p, idx, out, status);
-  HYTOPK_DISPATCH(p.d, p.dt, CALL);
-#undef CALL
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, uint32_t* status,
-                         cudaStream_t st) {
-  (void)status;
-  if (rows <= 0) return cudaSuccess;
-  const size_t smem = ((size_t)p.H * p.d + p.H) * 4;
-  const dim3 grid((p.L + kTileKeys - 1) / kTileKeys, (rows + kFilterQueries - 1) / kFilterQueries);
-  cudaError_t e = cudaSuccess;
-#define CALL(D, DT)                                     \
-  e = set_smem(k_table_simt<D, DT>, smem);              \
-  if (e == cudaSuccess) k_table_simt<D, DT><<<grid, 128, smem, st>>>(p, row0, rows, table);
   HYTOPK_DISPATCH(p.d, p.dt, CALL);
 #undef CALL
   if (e != cudaSuccess) return e;

@@ -1,0 +1,450 @@
+// stream_engine.cuh -- the tensor-core scoring engine over contiguous key
+// tiles: the fused score + threshold filter of HyTopK (no score table) and
+// the score-table writer of the two-pass path.
+//
+// HyScale explainer, HyTopK paragraph: the scoring kernel compares each score
+// with the query's threshold on chip and writes only passing keys into a
+// small per-query candidate buffer (atomic appends). Score-table paragraph:
+// the conventional method writes every score to HBM instead (MODE 1 here).
+//
+// Work item = (key chunk of 64 tiles x 128 keys, query block of QB slots).
+// One persistent CTA per SM walks items blockIdx.x, +gridDim.x, ... in
+// chunk-major order, so the CTAs running at one time share a key chunk in L2.
+//
+//   warp 0  TMA producer: the block's q rows (NG groups of 256 (query, head)
+//           rows) once per item, then the key tiles through a STAGES ring.
+//   warp 1  MMA issuer: per key tile and group, one 128 x 256 x d product
+//           (keys x (query, head)) into one of two TMEM accumulators.
+//   warp 2  TMEM allocator.
+//   warps 4..11 epilogue: TMEM lane = key, so each thread reduces its key's
+//           H heads per query in registers: ReLU, times w*q_scale (packed
+//           fp32 FMA), times k_scale; then the causal test and the threshold
+//           test, and a warp-aggregated append to the candidate buffer.
+#pragma once
+
+#include "tc.cuh"
+
+namespace hytopk {
+namespace stream {
+
+constexpr int kChunkTiles = 64;
+constexpr int kChunkKeys = kChunkTiles * kTileKeys;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 128 + kEpiWarps * 32;
+constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (and its 512 TMEM columns) per SM
+
+template <int D, int DT, int H>
+struct Cfg {
+  static constexpr int ES = DT == 0 ? 2 : 1;
+  static constexpr int RB = D * ES;
+  using Geo = tc::Geo<RB>;
+  static constexpr int G = 256 / H;               // queries per MMA (N = 256 columns)
+  static constexpr int NG = RB == 256 ? 1 : 2;    // MMA groups per work item
+  static constexpr int QB = G * NG;               // query slots per work item
+  static constexpr int KT_BYTES = 128 * RB;
+  static constexpr int QG_BYTES = 256 * RB;
+  static constexpr int STAGES = RB == 256 ? 3 : (RB == 128 ? 4 : 8);
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + NG * QG_BYTES;
+  static constexpr int BAR_OFF = K_OFF + STAGES * KT_BYTES;
+  static constexpr int NBARS = 2 * STAGES + 4 + 2;
+  static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;      // tmem base, abort flag
+  static constexpr int WQ_OFF = MISC_OFF + 16;
+  static constexpr int POS_OFF = WQ_OFF + QB * H * 4;
+  static constexpr int THR_OFF = POS_OFF + QB * 4;
+  static constexpr int ROW_OFF = THR_OFF + QB * 4;
+  static constexpr int END = ROW_OFF + QB * 4;
+  static constexpr int SMEM = (END + 1024) > kMinSmem ? (END + 1024) : kMinSmem;
+  static_assert(H >= 1 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two <= 128");
+  static_assert(RB == 64 || RB == 128 || RB == 256, "row bytes");
+};
+
+struct Args {
+  // MODE 0 (filter): slots sorted by position; plan = chunk offsets
+  const int32_t* qpos;
+  const float* thr;
+  const float* wq;
+  int32_t* cnt;
+  uint64_t* cand;
+  const int32_t* plan;  // [nchunks + 1] item offsets per key chunk
+  int C;
+  int n_pad;
+  int reverse;
+  // MODE 1 (table): original queries row0..row0+rows-1
+  const float* w;
+  const float* q_scale;
+  const int32_t* positions;
+  float* table;
+  int row0, rows, n;
+  // shared
+  const float* k_scale;
+  int L;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ int find_chunk(const int32_t* off, int nchunks, int item) {
+  int lo = 0, hi = nchunks - 1;  // largest c with off[c] <= item
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(off + mid) <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct Item {
+  int block, tile0, ntiles;
+};
+
+template <int QB, int MODE>
+__device__ __forceinline__ Item decode(const Args& a, int nchunks, int nblocks, int it) {
+  Item r;
+  int c;
+  if (MODE == 0) {
+    c = find_chunk(a.plan, nchunks, it);
+    r.block = it - __ldg(a.plan + c);
+    const int maxpos = __ldg(a.qpos + r.block * QB);
+    r.tile0 = c * kChunkTiles;
+    const int end = min(maxpos + 1, a.L);
+    r.ntiles = min(kChunkTiles, (end - r.tile0 * kTileKeys + kTileKeys - 1) / kTileKeys);
+  } else {
+    c = it / nblocks;
+    r.block = it - c * nblocks;
+    r.tile0 = c * kChunkTiles;
+    r.ntiles = min(kChunkTiles, (a.L - r.tile0 * kTileKeys + kTileKeys - 1) / kTileKeys);
+  }
+  return r;
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32)); }
+
+// Canonical head reduction, shared by every scoring kernel of the library:
+// head pair p = (2p, 2p+1) accumulates into packed accumulator p % NA with a
+// packed fp32 FMA of max(x, 0) and the folded weight; then
+// total = ((s0 + s1) + (s2 + s3)) with s_i = acc_i.x + acc_i.y.
+template <int H>
+struct HeadSum {
+  static constexpr int NA = H >= 8 ? 4 : (H >= 2 ? H / 2 : 1);
+  float a[2 * NA];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < 2 * NA; ++i) a[i] = 0.0f;
+  }
+  // heads h, h+1 (h even)
+  __device__ __forceinline__ void add_pair(int h, float x0, float x1, float w0, float w1) {
+    const int s = (h >> 1) % NA;
+    tc::fma2(a[2 * s], a[2 * s + 1], fmaxf(x0, 0.0f), fmaxf(x1, 0.0f), w0, w1);
+  }
+  __device__ __forceinline__ float total() const {
+    if (NA == 4) {
+      const float s0 = a[0] + a[1], s1 = a[2] + a[3], s2 = a[4] + a[5], s3 = a[6] + a[7];
+      return (s0 + s1) + (s2 + s3);
+    } else if (NA == 2) {
+      return (a[0] + a[1]) + (a[2] + a[3]);
+    } else {
+      return a[0] + a[1];
+    }
+  }
+};
+
+template <int H>
+__device__ __forceinline__ float single_head_score(float x, float w) {
+  return fmaxf(x, 0.0f) * w;
+}
+
+// Append (score, key) to slot's candidate buffer; all 32 lanes call it.
+__device__ __forceinline__ void append(bool pass, float score, int s, int slot, int32_t* cnt,
+                                       uint64_t* cand, int C) {
+  const unsigned mask = __ballot_sync(0xffffffffu, pass);
+  if (mask == 0u) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(mask) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(cnt + slot, __popc(mask));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (pass) {
+    const int at = base + __popc(mask & ((1u << lane) - 1u));
+    if (at < C) cand[(size_t)slot * C + at] = cand_key(score, s);
+  }
+}
+
+template <int D, int DT, int H, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_stream(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+             const Args a) {
+  using C_ = Cfg<D, DT, H>;
+  using Geo = typename C_::Geo;
+  constexpr int G = C_::G, NG = C_::NG, QB = C_::QB, STAGES = C_::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::BAR_OFF);
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;       // [2]
+  uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2]
+  uint64_t* q_full = bars + 2 * STAGES + 4;
+  uint64_t* q_empty = bars + 2 * STAGES + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C_::MISC_OFF + 4);
+  float* wq_s = reinterpret_cast<float*>(smem + C_::WQ_OFF);
+  int32_t* pos_s = reinterpret_cast<int32_t*>(smem + C_::POS_OFF);
+  float* thr_s = reinterpret_cast<float*>(smem + C_::THR_OFF);
+  int32_t* row_s = reinterpret_cast<int32_t*>(smem + C_::ROW_OFF);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunks = (a.L + kChunkKeys - 1) / kChunkKeys;
+  const int nblocks = MODE == 0 ? a.n_pad / QB : (a.rows + QB - 1) / QB;
+  const int total = MODE == 0 ? __ldg(a.plan + nchunks) : nchunks * nblocks;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      tc::mbar_init(k_full + i, 1);
+      tc::mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(acc_full + i, 1);
+      tc::mbar_init(acc_empty + i, kEpiWarps);
+    }
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 2) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto item_at = [&](int i) { return a.reverse ? total - 1 - i : i; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tc::tma_prefetch(&kmap);
+      tc::tma_prefetch(&qmap);
+      int stage = 0;
+      uint32_t sphase = 0, qphase = 0;
+      uint32_t pending = 0, pend_phase = 0, q_loads = 0;  // issued loads, for a clean abort
+      for (int i = blockIdx.x; i < total; i += gridDim.x) {
+        const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
+        if (!tc::mbar_wait(q_empty, qphase ^ 1u, abort_flag, a.status)) break;
+        qphase ^= 1u;
+        tc::mbar_expect_tx(q_full, NG * C_::QG_BYTES);
+        const int qrow0 = (MODE == 0 ? itm.block * QB : a.row0 + itm.block * QB) * H;
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+          for (int at = 0; at < Geo::kAtoms; ++at)
+            tc::tma_load_2d(smem + C_::Q_OFF + g * C_::QG_BYTES + at * 256 * Geo::kAtom, &qmap,
+                            q_full, at * Geo::kAtom / C_::ES, qrow0 + g * 256);
+        ++q_loads;
+        bool ok = true;
+        for (int t = 0; t < itm.ntiles; ++t) {
+          if (!tc::mbar_wait(k_empty + stage, sphase ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_expect_tx(k_full + stage, C_::KT_BYTES);
+#pragma unroll
+          for (int at = 0; at < Geo::kAtoms; ++at)
+            tc::tma_load_2d(smem + C_::K_OFF + stage * C_::KT_BYTES + at * 128 * Geo::kAtom,
+                            &kmap, k_full + stage, at * Geo::kAtom / C_::ES,
+                            (itm.tile0 + t) * kTileKeys);
+          pending |= 1u << stage;
+          pend_phase = (pend_phase & ~(1u << stage)) | (sphase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (*abort_flag) {
+        // let the copies still in flight land before the CTA exits (bounded)
+        const uint64_t t0 = tc::global_ns();
+        for (int st = 0; st < STAGES; ++st)
+          if (pending & (1u << st))
+            while (!tc::mbar_try_wait(k_full + st, (pend_phase >> st) & 1u) &&
+                   tc::global_ns() - t0 < 200000000ull) {
+            }
+        if (q_loads)
+          while (!tc::mbar_try_wait(q_full, (q_loads - 1) & 1u) &&
+                 tc::global_ns() - t0 < 200000000ull) {
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t IDESC = tc::instr_desc(DT, 128, 256);
+      const uint32_t q_addr = tc::smem_u32(smem + C_::Q_OFF);
+      const uint32_t k_addr = tc::smem_u32(smem + C_::K_OFF);
+      int stage = 0, acc = 0;
+      uint32_t sphase = 0, aphase = 0, qphase = 0;
+      for (int i = blockIdx.x; i < total; i += gridDim.x) {
+        const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
+        if (!tc::mbar_wait(q_full, qphase, abort_flag, a.status)) break;
+        qphase ^= 1u;
+        tc::fence_after_sync();
+        bool ok = true;
+        for (int t = 0; t < itm.ntiles && ok; ++t) {
+          if (!tc::mbar_wait(k_full + stage, sphase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            if (!tc::mbar_wait(acc_empty + acc, aphase ^ 1u, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+#pragma unroll
+            for (int j = 0; j < Geo::kSteps; ++j) {
+              const uint64_t adesc = tc::smem_desc(
+                  k_addr + stage * C_::KT_BYTES + Geo::step_offset(j, 128), Geo::kSbo, Geo::kSwizzle);
+              const uint64_t bdesc = tc::smem_desc(
+                  q_addr + g * C_::QG_BYTES + Geo::step_offset(j, 256), Geo::kSbo, Geo::kSwizzle);
+              tc::mma<DT>(d_tmem, adesc, bdesc, IDESC, j > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(acc_full + acc);
+            acc ^= 1;
+            if (acc == 0) aphase ^= 1u;
+          }
+          tc::mma_commit(k_empty + stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            sphase ^= 1u;
+          }
+        }
+        tc::mma_commit(q_empty);
+        if (!ok) break;
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int e = warp - 4;
+    const int quad = warp & 3;
+    const int half = e >> 2;
+    const int et = threadIdx.x - 128;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (int i = blockIdx.x; i < total; i += gridDim.x) {
+      const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
+      epi_sync();
+      for (int j = et; j < QB * H; j += kEpiWarps * 32) {
+        const int jb = j / H, h = j % H;
+        float wv;
+        if (MODE == 0) {
+          wv = __ldg(a.wq + (size_t)(itm.block * QB + jb) * H + h);
+        } else {
+          const int r = itm.block * QB + jb;
+          const int t = a.row0 + r;
+          wv = 0.0f;
+          if (r < a.rows) {
+            wv = __ldg(a.w + (size_t)t * H + h);
+            if (DT == 1) wv *= __ldg(a.q_scale + (size_t)t * H + h);
+          }
+        }
+        wq_s[j] = wv;
+      }
+      for (int jb = et; jb < QB; jb += kEpiWarps * 32) {
+        if (MODE == 0) {
+          const int slot = itm.block * QB + jb;
+          pos_s[jb] = __ldg(a.qpos + slot);
+          thr_s[jb] = __ldg(a.thr + slot);
+          row_s[jb] = slot;
+        } else {
+          const int r = itm.block * QB + jb;
+          int p = -1;
+          if (r < a.rows) {
+            p = __ldg(a.positions + a.row0 + r);
+            if (p < 0 || p >= a.L) p = -1;
+          }
+          pos_s[jb] = p;
+          row_s[jb] = r < a.rows ? r : -1;
+        }
+      }
+      epi_sync();
+      if (*abort_flag) continue;  // keep the named-barrier count equal across warps
+      bool ok = true;
+      for (int t = 0; t < itm.ntiles && ok; ++t) {
+        const int s = (itm.tile0 + t) * kTileKeys + quad * 32 + lane;
+        const float ks = DT == 1 ? (s < a.L ? __ldg(a.k_scale + s) : 0.0f) : 1.0f;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          if (!tc::mbar_wait(acc_full + acc, aphase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t tbase =
+              tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + half * 128);
+          // this warp's 128 columns = queries qlo .. qlo + 128/H - 1 of group g
+          const int qlo = g * G + (half * 128) / H;
+          HeadSum<H> hs;
+          hs.reset();
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            float v[64];
+            tc::tmem_ld64(tbase + ch * 64, v);
+            tc::tmem_wait_ld(v);
+#pragma unroll
+            for (int j = 0; j < 64; j += (H == 1 ? 1 : 2)) {
+              const int col = ch * 64 + j;       // column within this warp's half
+              const int jb = qlo + col / H;      // query slot within the block
+              const int h = col % H;
+              float sc;
+              bool done;
+              if (H == 1) {
+                sc = single_head_score<H>(v[j], wq_s[jb]);
+                done = true;
+              } else {
+                const float2 w2 = *reinterpret_cast<const float2*>(wq_s + jb * H + h);
+                hs.add_pair(h, v[j], v[j + 1], w2.x, w2.y);
+                done = (h + 2 == H);
+                if (done) {
+                  sc = hs.total();
+                  hs.reset();
+                }
+              }
+              if (done) {
+                sc = finish_score(sc, ks);
+                const int p = pos_s[jb];
+                if (MODE == 0) {
+                  const bool pass = (s <= p) && (sc >= thr_s[jb]);
+                  append(pass, sc, s, row_s[jb], a.cnt, a.cand, a.C);
+                } else {
+                  const int r = row_s[jb];
+                  if (r >= 0 && s < a.L)
+                    a.table[(size_t)r * a.L + s] = (s <= p) ? sc : -__int_as_float(0x7f800000);
+                }
+              }
+            }
+          }
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(acc_empty + acc);
+          acc ^= 1;
+          if (acc == 0) aphase ^= 1u;
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace stream
+}  // namespace hytopk

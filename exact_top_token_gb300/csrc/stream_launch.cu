@@ -1,0 +1,95 @@
+// stream_launch.cu -- host launchers of the streaming engine: the fused
+// score + filter phase of hytopk_select and the table writer of the two-pass
+// path.
+#include "launch.h"
+#include "stream_engine.cuh"
+
+namespace hytopk {
+
+cudaError_t launch_stream_d64_bf16(int H, int mode, const CUtensorMap& km, const CUtensorMap& qm,
+                                   const stream::Args& a, int grid, cudaStream_t st);
+cudaError_t launch_stream_d64_e4m3(int H, int mode, const CUtensorMap& km, const CUtensorMap& qm,
+                                   const stream::Args& a, int grid, cudaStream_t st);
+cudaError_t launch_stream_d128_bf16(int H, int mode, const CUtensorMap& km, const CUtensorMap& qm,
+                                    const stream::Args& a, int grid, cudaStream_t st);
+cudaError_t launch_stream_d128_e4m3(int H, int mode, const CUtensorMap& km, const CUtensorMap& qm,
+                                    const stream::Args& a, int grid, cudaStream_t st);
+
+namespace {
+
+int row_bytes(const Problem& p) { return p.d * (p.dt == 0 ? 2 : 1); }
+int atom_bytes(const Problem& p) { return row_bytes(p) >= 128 ? 128 : 64; }
+
+cudaError_t dispatch(const Problem& p, int mode, const CUtensorMap& km, const CUtensorMap& qm,
+                     const stream::Args& a, int grid, cudaStream_t st) {
+  if (p.d == 64)
+    return p.dt == 0 ? launch_stream_d64_bf16(p.H, mode, km, qm, a, grid, st)
+                     : launch_stream_d64_e4m3(p.H, mode, km, qm, a, grid, st);
+  return p.dt == 0 ? launch_stream_d128_bf16(p.H, mode, km, qm, a, grid, st)
+                   : launch_stream_d128_e4m3(p.H, mode, km, qm, a, grid, st);
+}
+
+bool key_map(const Problem& p, CUtensorMap* km) {
+  const int es = p.dt == 0 ? 2 : 1;
+  return make_tmap_2d(km, p.k, p.dt, (uint64_t)p.d, (uint64_t)p.L, atom_bytes(p) / es, 128,
+                      atom_bytes(p));
+}
+
+}  // namespace
+
+int stream_query_block(int H, int d, int dt) {
+  const int rb = d * (dt == 0 ? 2 : 1);
+  return (256 / H) * (rb == 256 ? 1 : 2);
+}
+
+cudaError_t launch_filter(const Problem& p, const SelectWs& ws, int reverse, cudaStream_t st) {
+  if (ws.n_pad == 0) return cudaSuccess;
+  const int es = p.dt == 0 ? 2 : 1;
+  CUtensorMap km, qm;
+  if (!key_map(p, &km)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&qm, ws.qp, p.dt, (uint64_t)p.d, (uint64_t)ws.n_pad * p.H,
+                    atom_bytes(p) / es, 256, atom_bytes(p)))
+    return cudaErrorInvalidValue;
+  const int qb = stream_query_block(p.H, p.d, p.dt);
+  cudaError_t e = launch_plan(ws, p.L, qb, st);
+  if (e != cudaSuccess) return e;
+  stream::Args a{};
+  a.qpos = ws.qpos;
+  a.thr = ws.thr;
+  a.wq = ws.wq;
+  a.cnt = ws.cnt;
+  a.cand = ws.cand;
+  a.plan = ws.plan;
+  a.C = ws.C;
+  a.n_pad = ws.n_pad;
+  a.reverse = reverse;
+  a.k_scale = p.k_scale;
+  a.L = p.L;
+  a.status = ws.counters + kCtrStatus;
+  return dispatch(p, 0, km, qm, a, num_sms(), st);
+}
+
+cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, uint32_t* status,
+                         cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const int es = p.dt == 0 ? 2 : 1;
+  CUtensorMap km, qm;
+  if (!key_map(p, &km)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&qm, p.q, p.dt, (uint64_t)p.d, (uint64_t)p.n * p.H, atom_bytes(p) / es, 256,
+                    atom_bytes(p)))
+    return cudaErrorInvalidValue;
+  stream::Args a{};
+  a.w = p.w;
+  a.q_scale = p.q_scale;
+  a.positions = p.positions;
+  a.table = table;
+  a.row0 = row0;
+  a.rows = rows;
+  a.n = p.n;
+  a.k_scale = p.k_scale;
+  a.L = p.L;
+  a.status = status;
+  return dispatch(p, 1, km, qm, a, num_sms(), st);
+}
+
+}  // namespace hytopk
