@@ -1,0 +1,395 @@
+// gather_engine.cuh -- the tensor-core scoring engine over gathered keys, one
+// query at a time: the sampled threshold of HyTopK, selection replay, and the
+// recovery rescoring of failed queries.
+//
+// HyScale explainer: the HyTopK paragraph (sample evenly spaced keys of the
+// query's own context, threshold at the sample that stands for about the 3k-th
+// key; small recovery kernels rescore failed queries over their whole
+// context), the worked example (M and r), and the selection-replay paragraph
+// (rescore only the k stored entries).
+//
+// Per query: the key rows it needs (samples, stored indices or its whole
+// prefix) are gathered 128 at a time with cp.async into swizzled shared
+// memory; one elected thread multiplies each 128-key tile by the query's
+// H x d operand (tcgen05, N = max(H, 16)); four epilogue warps (TMEM lane =
+// key) reduce the heads with the same arithmetic as the streaming engine.
+// The CTA then finishes the query together: the r-th best sample (threshold),
+// nothing (replay), or an exact top-k of the rescored row (recovery).
+//
+//   warps 0..3  producers (cp.async gather, 128 threads)
+//   warp 4      MMA issuer; warp 5 TMEM allocator
+//   warps 8..11 epilogue
+#pragma once
+
+#include "radix.cuh"
+#include "stream_engine.cuh"
+
+namespace hytopk {
+namespace gather {
+
+constexpr int kThreads = 384;
+constexpr int kProducers = 128;
+constexpr int kEpiFirstWarp = 8;
+constexpr int kSlots = 2;  // TMEM accumulators
+
+enum Mode { kThreshold = 0, kReplay = 1, kRecover = 2 };
+
+template <int D, int DT, int H, int MODE>
+struct Cfg {
+  static constexpr int ES = DT == 0 ? 2 : 1;
+  static constexpr int RB = D * ES;
+  using Geo = tc::Geo<RB>;
+  static constexpr int NQ = H < 16 ? 16 : H;         // MMA N (query rows, zero padded)
+  static constexpr int CPR = RB / 16;                // 16-byte chunks per row
+  static constexpr int STAGES = RB == 256 ? 3 : 4;
+  static constexpr int KT_BYTES = 128 * RB;
+  static constexpr int RING = STAGES * KT_BYTES;
+  static constexpr int TMEM_COLS = (kSlots * NQ) < 32 ? 32 : (kSlots * NQ);
+  static constexpr int Q_OFF = 0;
+  static constexpr int U_OFF = ((NQ * RB + 1023) / 1024) * 1024;  // stage ring / post scratch
+  static constexpr int NBARS = 2 * STAGES + 2 * kSlots;
+  // host computes the union size (depends on k for recovery)
+  static_assert(H >= 1 && H <= 128 && (H & (H - 1)) == 0, "H");
+};
+
+struct GArgs {
+  // the problem
+  const void* k;
+  const float* k_scale;
+  int L, k_top, n;
+  // threshold / recovery: packed slots
+  const int32_t* perm;
+  const int32_t* qpos;
+  const void* qp;
+  const float* wq;
+  float* thr;
+  const float* override_thr;
+  int n_pad;
+  // replay: original queries
+  const void* q;
+  const float* q_scale;
+  const float* w;
+  const int32_t* idx;
+  float* out;
+  // recovery
+  uint32_t* counters;
+  const int32_t* failed_list;
+  float* rowbuf;
+  uint64_t* rowlist;
+  int32_t* idx_out;
+  float* scores_out;
+  // layout
+  int u_bytes;  // size of the stage-ring / post-processing union
+  uint32_t* status;
+};
+
+template <int D, int DT, int H, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) k_gather(const GArgs a) {
+  using C_ = Cfg<D, DT, H, MODE>;
+  using Geo = typename C_::Geo;
+  constexpr int NQ = C_::NQ, STAGES = C_::STAGES, CPR = C_::CPR, RB = C_::RB;
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* qbuf = smem + C_::Q_OFF;
+  uint8_t* ring = smem + C_::U_OFF;
+  uint8_t* tail = ring + a.u_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* acc_full = bars + 2 * STAGES;
+  uint64_t* acc_empty = bars + 2 * STAGES + kSlots;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(bars + C_::NBARS);
+  uint32_t* tmem_slot = misc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  int* item_sh = reinterpret_cast<int*>(misc + 2);
+  float* wq_s = reinterpret_cast<float*>(misc + 4);              // [H]
+  uint32_t* keys_s = reinterpret_cast<uint32_t*>(wq_s + 128);    // [kMaxSamples] (threshold)
+  RadixScratch& rsc = *reinterpret_cast<RadixScratch*>(ring);    // after the pipeline drains
+  uint64_t* sel = reinterpret_cast<uint64_t*>(ring + sizeof(RadixScratch));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      tc::mbar_init(full + i, kProducers);
+      tc::mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      tc::mbar_init(acc_full + i, 1);
+      tc::mbar_init(acc_empty + i, 4);
+    }
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 5) {
+    tc::tmem_alloc(tmem_slot, C_::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // pipeline state, continued across queries by each role
+  int p_stage = 0, m_stage = 0, m_slot = 0, e_slot = 0;
+  uint32_t p_phase = 0, m_phase = 0, m_aphase = 0, e_aphase = 0;
+
+  const int n_items = MODE == kThreshold ? a.n_pad : (MODE == kReplay ? a.n : 0);
+  const uint32_t n_failed = MODE == kRecover ? a.counters[kCtrFailed] : 0u;
+  const bool fallback = n_failed > HYTOPK_MAX_RECOVERY_ROWS;
+  const int n_rec = MODE == kRecover ? (fallback ? a.n_pad : (int)n_failed) : 0;
+
+  for (int it = blockIdx.x;; it += gridDim.x) {
+    // ---- pick the query (uniform across the CTA) ----
+    int item;
+    if (MODE == kRecover) {
+      if (threadIdx.x == 0) *item_sh = (int)atomicAdd(a.counters + kCtrRecoverWork, 1u);
+      __syncthreads();
+      item = *item_sh;
+      __syncthreads();
+      if (item >= n_rec) break;
+    } else {
+      item = it;
+      if (item >= n_items) break;
+    }
+    if (*abort_flag) break;
+    int slot = -1, t = -1, ctx = 0, nrows = 0, M = 0, r = 0;
+    if (MODE == kReplay) {
+      t = item;
+      nrows = a.k_top;
+    } else {
+      slot = MODE == kThreshold ? item : (fallback ? item : a.failed_list[item]);
+      t = a.perm[slot];
+      ctx = a.qpos[slot] + 1;
+      if (t < 0) continue;
+      if (MODE == kThreshold) {
+        if (ctx <= a.k_top || a.override_thr) {
+          if (threadIdx.x == 0)
+            a.thr[slot] = ctx <= a.k_top ? -__int_as_float(0x7f800000) : a.override_thr[t];
+          continue;
+        }
+        M = sample_count(ctx);
+        r = threshold_rank(ctx, a.k_top, M);
+        nrows = M;
+      } else {
+        nrows = ctx;
+      }
+    }
+    const int ntiles = (nrows + kTileKeys - 1) / kTileKeys;
+
+    // ---- the query operand (H rows of d, zero-padded to NQ) and weights ----
+    {
+      const uint8_t* qsrc =
+          MODE == kReplay ? reinterpret_cast<const uint8_t*>(a.q) + (size_t)t * H * RB
+                          : reinterpret_cast<const uint8_t*>(a.qp) + (size_t)slot * H * RB;
+      for (int f = threadIdx.x; f < NQ * CPR; f += kThreads) {
+        const int row = f / CPR, c = f % CPR;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < H) v = *reinterpret_cast<const uint4*>(qsrc + (size_t)row * RB + c * 16);
+        *reinterpret_cast<uint4*>(qbuf + Geo::chunk_offset(row, c, NQ)) = v;
+      }
+      for (int h = threadIdx.x; h < H; h += kThreads) {
+        float wv;
+        if (MODE == kReplay) {
+          wv = a.w[(size_t)t * H + h];
+          if (DT == 1) wv *= a.q_scale[(size_t)t * H + h];
+        } else {
+          wv = a.wq[(size_t)slot * H + h];
+        }
+        wq_s[h] = wv;
+      }
+      tc::fence_proxy_async_smem();
+      __syncthreads();
+    }
+
+    if (warp < 4) {
+      // ---------------- producers: gather 128 key rows per tile ----------------
+      const int tid = threadIdx.x;
+      int npend = 0;
+      for (int i = 0; i < ntiles; ++i) {
+        if (!tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status)) break;
+        uint8_t* dst = ring + p_stage * C_::KT_BYTES;
+        for (int f = tid; f < kTileKeys * CPR; f += kProducers) {
+          const int row = f / CPR, c = f % CPR;
+          const int j = i * kTileKeys + row;
+          int s = -1;
+          if (j < nrows) {
+            if (MODE == kThreshold) s = sample_position(ctx, M, j);
+            else if (MODE == kReplay) {
+              s = __ldg(a.idx + (size_t)t * a.k_top + j);
+              if (s < 0 || s >= a.L) s = -1;
+            } else s = j;
+          }
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.k) +
+                               (s >= 0 ? (size_t)s * RB + c * 16 : 0);
+          tc::cp_async16(dst + Geo::chunk_offset(row, c, kTileKeys), src, s >= 0);
+        }
+        tc::cp_async_commit();
+        ++npend;
+        if (npend == STAGES - 1) {
+          tc::cp_async_wait<STAGES - 2>();
+          tc::fence_proxy_async_smem();
+          const int st = (p_stage - (npend - 1) + STAGES) % STAGES;
+          tc::mbar_arrive(full + st);
+          --npend;
+        }
+        if (++p_stage == STAGES) {
+          p_stage = 0;
+          p_phase ^= 1u;
+        }
+      }
+      tc::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      for (; npend > 0; --npend) tc::mbar_arrive(full + (p_stage - npend + STAGES) % STAGES);
+    } else if (warp == 4) {
+      if (lane == 0) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t IDESC = tc::instr_desc(DT, 128, NQ);
+        const uint32_t q_addr = tc::smem_u32(qbuf);
+        const uint32_t r_addr = tc::smem_u32(ring);
+        for (int i = 0; i < ntiles; ++i) {
+          if (!tc::mbar_wait(full + m_stage, m_phase, abort_flag, a.status)) break;
+          tc::fence_after_sync();
+          if (!tc::mbar_wait(acc_empty + m_slot, m_aphase ^ 1u, abort_flag, a.status)) break;
+          tc::fence_after_sync();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(m_slot * NQ);
+#pragma unroll
+          for (int j = 0; j < Geo::kSteps; ++j) {
+            const uint64_t adesc = tc::smem_desc(
+                r_addr + m_stage * C_::KT_BYTES + Geo::step_offset(j, kTileKeys), Geo::kSbo,
+                Geo::kSwizzle);
+            const uint64_t bdesc =
+                tc::smem_desc(q_addr + Geo::step_offset(j, NQ), Geo::kSbo, Geo::kSwizzle);
+            tc::mma<DT>(d_tmem, adesc, bdesc, IDESC, j > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(acc_full + m_slot);
+          tc::mma_commit(empty + m_stage);
+          if (++m_stage == STAGES) {
+            m_stage = 0;
+            m_phase ^= 1u;
+          }
+          if (++m_slot == kSlots) {
+            m_slot = 0;
+            m_aphase ^= 1u;
+          }
+        }
+      }
+    } else if (warp >= kEpiFirstWarp) {
+      // ---------------- epilogue: one key per thread ----------------
+      const int quad = warp & 3;
+      const int row = quad * 32 + lane;
+      for (int i = 0; i < ntiles; ++i) {
+        if (!tc::mbar_wait(acc_full + e_slot, e_aphase, abort_flag, a.status)) break;
+        tc::fence_after_sync();
+        const uint32_t taddr =
+            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(e_slot * NQ);
+        const int j = i * kTileKeys + row;
+        int s = -1;
+        if (j < nrows) {
+          if (MODE == kThreshold) s = sample_position(ctx, M, j);
+          else if (MODE == kReplay) s = __ldg(a.idx + (size_t)t * a.k_top + j);
+          else s = j;
+        }
+        const bool valid = s >= 0 && s < a.L;
+        const float ks = DT == 1 ? (valid ? __ldg(a.k_scale + s) : 0.0f) : 1.0f;
+        stream::HeadSum<H> hs;
+        hs.reset();
+        float sc;
+        if (H >= 64) {
+#pragma unroll
+          for (int c0 = 0; c0 < H; c0 += 64) {
+            float v[64];
+            tc::tmem_ld64(taddr + c0, v);
+            tc::tmem_wait_ld(v);
+#pragma unroll
+            for (int h = 0; h < 64; h += 2) hs.add_pair(c0 + h, v[h], v[h + 1], wq_s[c0 + h], wq_s[c0 + h + 1]);
+          }
+          sc = hs.total();
+        } else if (H == 32) {
+          float v[32];
+          tc::tmem_ld32(taddr, v);
+          tc::tmem_wait_ld(v);
+#pragma unroll
+          for (int h = 0; h < 32; h += 2) hs.add_pair(h, v[h], v[h + 1], wq_s[h], wq_s[h + 1]);
+          sc = hs.total();
+        } else {
+          float v[16];
+          tc::tmem_ld16(taddr, v);
+          tc::tmem_wait_ld(v);
+          if (H == 1) {
+            sc = stream::single_head_score<H>(v[0], wq_s[0]);
+          } else {
+#pragma unroll
+            for (int h = 0; h < (H < 16 ? H : 16); h += 2)
+              hs.add_pair(h, v[h], v[h + 1], wq_s[h], wq_s[h + 1]);
+            sc = hs.total();
+          }
+        }
+        sc = finish_score(sc, ks);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(acc_empty + e_slot);
+        if (++e_slot == kSlots) {
+          e_slot = 0;
+          e_aphase ^= 1u;
+        }
+        if (j < nrows) {
+          if (MODE == kThreshold) {
+            keys_s[j] = desc32(sc);
+          } else if (MODE == kReplay) {
+            float v = sc;
+            if (!valid) {
+              if (s == -1) {
+                v = -__int_as_float(0x7f800000);
+              } else {
+                v = __int_as_float(0x7fc00000);
+                if (a.status) atomicOr(a.status, HYTOPK_DEV_REPLAY_BAD_INDEX);
+              }
+            }
+            a.out[(size_t)t * a.k_top + j] = v;
+          } else {
+            a.rowbuf[(size_t)blockIdx.x * a.L + j] = sc;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (*abort_flag) break;
+    // ---- per-query completion (whole CTA) ----
+    if (MODE == kThreshold) {
+      const uint32_t v = cta_kth_smallest_u32(keys_s, M, (uint32_t)r, rsc);
+      if (threadIdx.x == 0) a.thr[slot] = desc32_score(v);
+      __syncthreads();
+    } else if (MODE == kRecover) {
+      const int got = cta_row_topk(a.rowbuf + (size_t)blockIdx.x * a.L, ctx, a.k_top,
+                                   a.rowlist + (size_t)blockIdx.x * a.L, sel, rsc);
+      write_selection(sel, got, a.k_top, a.idx_out + (size_t)t * a.k_top,
+                      a.scores_out ? a.scores_out + (size_t)t * a.k_top : nullptr);
+      __syncthreads();
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, C_::TMEM_COLS);
+  }
+}
+
+// Shared memory of k_gather: q operand + max(stage ring, post-processing
+// scratch) + barriers, weights and (threshold) the sample keys.
+template <int D, int DT, int H, int MODE>
+inline int gather_smem_bytes(int k_top, int* u_bytes) {
+  using C_ = Cfg<D, DT, H, MODE>;
+  int post = 0;
+  if (MODE == kThreshold) post = (int)sizeof(RadixScratch);
+  if (MODE == kRecover) post = (int)sizeof(RadixScratch) + sort_capacity(k_top) * 8;
+  int u = C_::RING > post ? C_::RING : post;
+  u = (u + 15) / 16 * 16;
+  *u_bytes = u;
+  const int tail = 8 * C_::NBARS + 16 + 128 * 4 + (MODE == kThreshold ? kMaxSamples * 4 : 0);
+  return 1024 + C_::U_OFF + u + tail;
+}
+
+}  // namespace gather
+}  // namespace hytopk
