@@ -294,14 +294,15 @@ def gpu_arm(args, world, rank, local):
     flops_per_pair = 2 * H * d
     filter_s = phase_ms["filter"] / 1e3
     achieved_tflops = pairs * flops_per_pair / filter_s / 1e12
-    # first version scores on the CUDA cores: fp32 FMA roofline (152 SMs x 128 lanes x 2 flop)
-    alu_peak = 152 * 128 * 2 * (clk["sm_max_mhz"] if clk and clk.get("sm_max_mhz") else 2070) / 1e6
-    roofline = {"kernel": "k_filter (fused score + threshold filter)", "bound": "alu",
-                "achieved": achieved_tflops, "peak": alu_peak, "unit": "TFLOP/s",
-                "frac": achieved_tflops / alu_peak, "traffic": None,
+    # dense tensor peak of the input dtype: fp8 = 2 x the measured bf16 GEMM peak
+    # (the nominal fp8/bf16 ratio); bf16 = the measured bf16 peak
+    peak = pk["bf16_tflops"] * (2.0 if case["dtype"] == "e4m3" else 1.0)
+    roofline = {"kernel": "k_stream filter (fused score + threshold filter)", "bound": "tensor",
+                "achieved": achieved_tflops, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved_tflops / peak, "traffic": None,
                 "algorithmic_flops_per_launch": pairs * flops_per_pair,
-                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock",
-                "tensor_frac_fp8_of_measured": achieved_tflops / (2 * pk["bf16_tflops"])}
+                "peak_source": (f"{'2 x ' if case['dtype'] == 'e4m3' else ''}measured bf16 burst "
+                                f"{pk['bf16_tflops']} TFLOP/s ({pk['source']})")}
     replay_bytes = n * k_top * REPLAY_BYTES_PER_ENTRY[case["dtype"]]
     replay = {"entries_per_s": n * k_top / (replay_ms / 1e3), "ms": replay_ms,
               "achieved_gbs": replay_bytes / (replay_ms / 1e3) / 1e9,
