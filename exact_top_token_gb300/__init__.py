@@ -31,8 +31,8 @@ BF16, E4M3 = 0, 1
 
 # the C-ABI symbols declared in include/hytopk.h
 symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", "hytopk_replay",
-           "hytopk_twopass_workspace_size", "hytopk_select_twopass", "hytopk_status_string",
-           "hytopk_version")
+           "hytopk_twopass_workspace_size", "hytopk_select_twopass", "hytopk_select_noalloc",
+           "hytopk_status_string", "hytopk_version")
 
 
 class HytopkError(RuntimeError):

@@ -31,7 +31,8 @@
  * Conventions shared by every call:
  *   - Every array pointer is DEVICE memory owned by the caller. The library
  *     allocates nothing and keeps no state between calls; scratch memory is
- *     the caller's `workspace`.
+ *     the caller's `workspace` (hytopk_select_noalloc, for callers that
+ *     cannot provide one, uses a fixed array the library holds instead).
  *   - Calls are asynchronous on `stream` (0 = legacy default stream). The
  *     return code covers host-side argument checks and launch errors only;
  *     conditions found on the device are reported through the device status
@@ -192,6 +193,36 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
                                     int k_top, hytopk_dtype dt, int32_t* idx_out,
                                     float* scores_out, void* workspace, size_t workspace_bytes,
                                     uint32_t* dev_status, cudaStream_t stream);
+
+/* hytopk_select without a caller workspace, for callers that cannot allocate
+ * device memory: code inside a host framework that owns the whole device
+ * memory budget through its own pool and forbids other allocations, or
+ * latency-critical paths where an allocation (and the device synchronisation
+ * that cudaMalloc/cudaFree can imply) is not acceptable. The HyScale pages
+ * have no counterpart to this entry point; it only changes where the scratch
+ * memory comes from.
+ *   The scratch is one fixed array of HYTOPK_NOALLOC_SCRATCH_BYTES in device
+ *   memory, held by the library on every GPU that loads it until the process
+ *   exits. The entry point allocates nothing (no cudaMalloc, cudaFree or
+ *   allocating library call).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   A problem whose hytopk_select_workspace_size exceeds the array returns
+ *   HYTOPK_WORKSPACE_TOO_SMALL and launches nothing.
+ *   All calls share the one array and each call overwrites it (the call
+ *   itself clears what must start at zero), so calls whose GPU work overlaps
+ *   in time -- on different streams or host threads -- race; the caller must
+ *   order them.
+ * Arguments and outputs are those of hytopk_select. */
+#define HYTOPK_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+hytopk_status hytopk_select_noalloc(const void* q, const float* q_scale, const void* k,
+                                    const float* k_scale, const float* w,
+                                    const int32_t* positions, int n, int L, int H, int d,
+                                    int k_top, hytopk_dtype dt, int32_t* idx_out,
+                                    float* scores_out, int capacity, hytopk_stats* stats_out,
+                                    cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* hytopk_status_string(hytopk_status status);
