@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--no-twopass", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=48, help="oracle sample size (queries)")
+    ap.add_argument("--queries", type=int, default=0,
+                    help="keep only the last N queries of the workload (profiling captures)")
     return ap.parse_args()
 
 
@@ -231,6 +233,9 @@ def gpu_arm(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     case = WORKLOADS[args.workload]()
+    if args.queries:
+        case = si.subset(case, np.arange(len(case["positions"]) - args.queries,
+                                         len(case["positions"])))
     n, H, d = case["q"].shape
     L = case["k"].shape[0]
     k_top = case["k_top"]

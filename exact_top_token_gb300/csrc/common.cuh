@@ -26,7 +26,7 @@ namespace hytopk {
 constexpr int kTileKeys = 128;       // keys per scoring tile (one TMEM lane / thread each)
 constexpr int kQueryPad = 512;       // query slots are padded to a multiple of this
 constexpr int kMaxSamples = 8192;    // upper clamp of the sample count M
-constexpr int kRecoveryCtas = 128;   // persistent CTAs of the recovery kernel
+constexpr int kRecoveryCtas = 64;    // persistent CTAs of the recovery kernel (one row each)
 constexpr int kMaxTopK = 16384;
 
 // Counters kept in the workspace (zeroed at the start of every call).
