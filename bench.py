@@ -218,9 +218,9 @@ def workload_config(case):
 # ---- the GPU arm -------------------------------------------------------------------------
 
 def launches_per_step(dtype):
-    # select: rank, pack, [key-scale check], threshold, filter, check, select, recover;
-    # then one replay launch
-    return (8 if dtype == "e4m3" else 7) + 1
+    # select: rank, pack, [key-scale check], threshold, plan, filter, check, select,
+    # recover; then one replay launch
+    return (9 if dtype == "e4m3" else 8) + 1
 
 
 def gpu_arm(args, world, rank, local):

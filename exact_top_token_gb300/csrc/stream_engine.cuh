@@ -16,7 +16,7 @@
 //   warp 1  MMA issuer: per key tile and group, one 128 x 256 x d product
 //           (keys x (query, head)) into one of two TMEM accumulators.
 //   warp 2  TMEM allocator.
-//   warps 4..11 epilogue: TMEM lane = key, so each thread reduces its key's
+//   warps 4..19 epilogue: TMEM lane = key, so each thread reduces its key's
 //           H heads per query in registers: ReLU, times w*q_scale (packed
 //           fp32 FMA), times k_scale; then the causal test and the threshold
 //           test, and a warp-aggregated append to the candidate buffer.
@@ -29,7 +29,7 @@ namespace stream {
 
 constexpr int kChunkTiles = 64;
 constexpr int kChunkKeys = kChunkTiles * kTileKeys;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
 constexpr int kThreads = 128 + kEpiWarps * 32;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (and its 512 TMEM columns) per SM
 
@@ -55,6 +55,9 @@ struct Cfg {
   static constexpr int ROW_OFF = THR_OFF + QB * 4;
   static constexpr int END = ROW_OFF + QB * 4;
   static constexpr int SMEM = (END + 1024) > kMinSmem ? (END + 1024) : kMinSmem;
+  // epilogue: each warp owns one TMEM lane quadrant (32 keys) and CW columns
+  static constexpr int CW = H == 128 ? 128 : 64;
+  static constexpr int ACTIVE_EPI = 4 * (256 / CW);  // warps that read accumulators
   static_assert(H >= 1 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two <= 128");
   static_assert(RB == 64 || RB == 128 || RB == 256, "row bytes");
 };
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(acc_full + i, 1);
-      tc::mbar_init(acc_empty + i, kEpiWarps);
+      tc::mbar_init(acc_empty + i, C_::ACTIVE_EPI);
     }
     tc::mbar_init(q_full, 1);
     tc::mbar_init(q_empty, 1);
@@ -330,9 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
+    constexpr int CW = C_::CW;
     const int e = warp - 4;
     const int quad = warp & 3;
-    const int half = e >> 2;
+    const int sub = e >> 2;                 // column span of this warp: [sub*CW, sub*CW+CW)
+    const bool reads_tmem = sub * CW < 256;
     const int et = threadIdx.x - 128;
     int acc = 0;
     uint32_t aphase = 0;
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       epi_sync();
-      if (*abort_flag) continue;  // keep the named-barrier count equal across warps
+      if (*abort_flag || !reads_tmem) continue;  // named-barrier count stays equal
       bool ok = true;
       for (int t = 0; t < itm.ntiles && ok; ++t) {
         const int s = (itm.tile0 + t) * kTileKeys + quad * 32 + lane;
@@ -386,36 +391,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::fence_after_sync();
           const uint32_t tbase =
-              tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + half * 128);
-          // this warp's 128 columns = queries qlo .. qlo + 128/H - 1 of group g
-          const int qlo = g * G + (half * 128) / H;
+              tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + sub * CW);
+          // this warp's CW columns = queries qlo .. of group g (whole queries: CW % H == 0)
+          const int qlo = g * G + (sub * CW) / H;
           HeadSum<H> hs;
           hs.reset();
 #pragma unroll
-          for (int ch = 0; ch < 2; ++ch) {
-            float v[64];
-            tc::tmem_ld64(tbase + ch * 64, v);
+          for (int ch = 0; ch < CW / 32; ++ch) {
+            float v[32];
+            tc::tmem_ld32(tbase + ch * 32, v);
             tc::tmem_wait_ld(v);
+            constexpr int STEP = H == 1 ? 1 : (H == 2 ? 2 : 4);
 #pragma unroll
-            for (int j = 0; j < 64; j += (H == 1 ? 1 : 2)) {
-              const int col = ch * 64 + j;       // column within this warp's half
+            for (int j = 0; j < 32; j += STEP) {
+              const int col = ch * 32 + j;       // column within this warp's span
               const int jb = qlo + col / H;      // query slot within the block
               const int h = col % H;
-              float sc;
-              bool done;
+              float sc = 0.0f;
+              bool done = false;
               if (H == 1) {
                 sc = single_head_score<H>(v[j], wq_s[jb]);
                 done = true;
-              } else {
+              } else if (H == 2) {
                 const float2 w2 = *reinterpret_cast<const float2*>(wq_s + jb * H + h);
                 hs.add_pair(h, v[j], v[j + 1], w2.x, w2.y);
-                done = (h + 2 == H);
-                if (done) {
+                done = true;
+              } else {
+                const float4 w4 = *reinterpret_cast<const float4*>(wq_s + jb * H + h);
+                hs.add_pair(h, v[j], v[j + 1], w4.x, w4.y);
+                hs.add_pair(h + 2, v[j + 2], v[j + 3], w4.z, w4.w);
+                done = (h + 4 == H);
+              }
+              if (done) {
+                if (H >= 2) {
                   sc = hs.total();
                   hs.reset();
                 }
-              }
-              if (done) {
                 sc = finish_score(sc, ks);
                 const int p = pos_s[jb];
                 if (MODE == 0) {
