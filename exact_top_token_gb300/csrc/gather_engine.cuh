@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather(const GArgs a) {
         } else {
           wv = a.wq[(size_t)slot * H + h];
         }
-        wq_s[h] = wv;
+        wq_s[h] = 0.5f * wv;  // halved: see stream::HeadSum
       }
       tc::fence_proxy_async_smem();
       __syncthreads();

@@ -121,38 +121,45 @@ __device__ __forceinline__ Item decode(const Args& a, int nchunks, int nblocks, 
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32)); }
 
-// Canonical head reduction, shared by every scoring kernel of the library:
-// head pair p = (2p, 2p+1) accumulates into packed accumulator p % NA with a
-// packed fp32 FMA of max(x, 0) and the folded weight; then
-// total = ((s0 + s1) + (s2 + s3)) with s_i = acc_i.x + acc_i.y.
+// Canonical head reduction, shared by every scoring kernel of the library.
+// The weights are stored halved (hw = w / 2) and ReLU(x) * w is evaluated as
+// (x + |x|) * hw: 2x and w/2 are exact scalings, so the product is bit for
+// bit ReLU(x) * w (for |w| >= 2^-125), while the add runs on the FMA pipe.
+// Head pair p = (2p, 2p+1) accumulates into packed accumulator p % NA with
+// one packed fp32 FMA; then total = ((s0 + s1) + (s2 + s3)), s_i = lo_i + hi_i.
 template <int H>
 struct HeadSum {
   static constexpr int NA = H >= 8 ? 4 : (H >= 2 ? H / 2 : 1);
-  float a[2 * NA];
+  uint64_t a[NA];
   __device__ __forceinline__ void reset() {
 #pragma unroll
-    for (int i = 0; i < 2 * NA; ++i) a[i] = 0.0f;
+    for (int i = 0; i < NA; ++i) a[i] = 0ull;
   }
-  // heads h, h+1 (h even)
-  __device__ __forceinline__ void add_pair(int h, float x0, float x1, float w0, float w1) {
+  // heads h, h+1 (h even), halved weights hw0, hw1
+  __device__ __forceinline__ void add_pair(int h, float x0, float x1, float hw0, float hw1) {
     const int s = (h >> 1) % NA;
-    tc::fma2(a[2 * s], a[2 * s + 1], fmaxf(x0, 0.0f), fmaxf(x1, 0.0f), w0, w1);
+    const float r0 = x0 + fabsf(x0), r1 = x1 + fabsf(x1);
+    uint64_t r, w;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(r0), "f"(r1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(hw0), "f"(hw1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a[s]) : "l"(r), "l"(w));
+  }
+  __device__ __forceinline__ float lane_sum(int i) const {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a[i]));
+    return lo + hi;
   }
   __device__ __forceinline__ float total() const {
-    if (NA == 4) {
-      const float s0 = a[0] + a[1], s1 = a[2] + a[3], s2 = a[4] + a[5], s3 = a[6] + a[7];
-      return (s0 + s1) + (s2 + s3);
-    } else if (NA == 2) {
-      return (a[0] + a[1]) + (a[2] + a[3]);
-    } else {
-      return a[0] + a[1];
-    }
+    if (NA == 4) return (lane_sum(0) + lane_sum(1)) + (lane_sum(2) + lane_sum(3));
+    if (NA == 2) return lane_sum(0) + lane_sum(1);
+    return lane_sum(0);
   }
 };
 
+// H = 1: ReLU(x) * w with the halved weight, as above.
 template <int H>
-__device__ __forceinline__ float single_head_score(float x, float w) {
-  return fmaxf(x, 0.0f) * w;
+__device__ __forceinline__ float single_head_score(float x, float hw) {
+  return (x + fabsf(x)) * hw;
 }
 
 // Append (score, key) to slot's candidate buffer; all 32 lanes call it.
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (DT == 1) wv *= __ldg(a.q_scale + (size_t)t * H + h);
           }
         }
-        wq_s[j] = wv;
+        wq_s[j] = 0.5f * wv;  // halved: see HeadSum
       }
       for (int jb = et; jb < QB; jb += kEpiWarps * 32) {
         if (MODE == 0) {
@@ -380,9 +387,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       epi_sync();
       if (*abort_flag || !reads_tmem) continue;  // named-barrier count stays equal
       bool ok = true;
+      const int s_first = itm.tile0 * kTileKeys + quad * 32 + lane;
+      float ks_next = DT == 1 ? (s_first < a.L ? __ldg(a.k_scale + s_first) : 0.0f) : 1.0f;
       for (int t = 0; t < itm.ntiles && ok; ++t) {
         const int s = (itm.tile0 + t) * kTileKeys + quad * 32 + lane;
-        const float ks = DT == 1 ? (s < a.L ? __ldg(a.k_scale + s) : 0.0f) : 1.0f;
+        const float ks = ks_next;
+        if (DT == 1) {
+          const int sn = s + kTileKeys;
+          ks_next = (t + 1 < itm.ntiles && sn < a.L) ? __ldg(a.k_scale + sn) : 0.0f;
+        }
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           if (!tc::mbar_wait(acc_full + acc, aphase, abort_flag, a.status)) {
