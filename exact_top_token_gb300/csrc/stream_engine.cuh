@@ -33,7 +33,7 @@ constexpr int kEpiWarps = 16;
 constexpr int kThreads = 128 + kEpiWarps * 32;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (and its 512 TMEM columns) per SM
 
-template <int D, int DT, int H>
+template <int D, int DT, int H, int MODE_STAGING = 1>
 struct Cfg {
   static constexpr int ES = DT == 0 ? 2 : 1;
   static constexpr int RB = D * ES;
@@ -53,7 +53,11 @@ struct Cfg {
   static constexpr int POS_OFF = WQ_OFF + QB * H * 4;
   static constexpr int THR_OFF = POS_OFF + QB * 4;
   static constexpr int ROW_OFF = THR_OFF + QB * 4;
-  static constexpr int END = ROW_OFF + QB * 4;
+  // per-item candidate staging (filter): CAP entries per query slot of the block
+  static constexpr int STAGE_CAP = (1024 / QB) > 8 ? (1024 / QB) : 8;
+  static constexpr int SCNT_OFF = ROW_OFF + QB * 4;
+  static constexpr int STAGE_OFF = ((SCNT_OFF + QB * 4) + 15) / 16 * 16;
+  static constexpr int END = STAGE_OFF + (MODE_STAGING ? QB * STAGE_CAP * 8 : 0);
   static constexpr int SMEM = (END + 1024) > kMinSmem ? (END + 1024) : kMinSmem;
   // epilogue: each warp owns one TMEM lane quadrant (32 keys) and CW columns
   static constexpr int CW = H == 128 ? 128 : 64;
@@ -162,27 +166,61 @@ __device__ __forceinline__ float single_head_score(float x, float hw) {
   return (x + fabsf(x)) * hw;
 }
 
-// Append (score, key) to slot's candidate buffer; all 32 lanes call it.
-__device__ __forceinline__ void append(bool pass, float score, int s, int slot, int32_t* cnt,
-                                       uint64_t* cand, int C) {
+// Append (score, key) to the query's candidate buffer; all 32 lanes call it.
+// Candidates are staged per work item in shared memory (a shared atomic per
+// warp reserves room); the item's flush reserves global room with one atomic
+// per query. Entries beyond the staging capacity take the global path at once.
+template <int CAP>
+__device__ __forceinline__ void append_staged(bool pass, float score, int s, int jb, int slot,
+                                              uint32_t* scnt, uint64_t* stage, int32_t* cnt,
+                                              uint64_t* cand, int C) {
   const unsigned mask = __ballot_sync(0xffffffffu, pass);
   if (mask == 0u) return;
   const int lane = threadIdx.x & 31;
   const int leader = __ffs(mask) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(cnt + slot, __popc(mask));
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(scnt + jb, (uint32_t)__popc(mask));
   base = __shfl_sync(0xffffffffu, base, leader);
   if (pass) {
-    const int at = base + __popc(mask & ((1u << lane) - 1u));
-    if (at < C) cand[(size_t)slot * C + at] = cand_key(score, s);
+    const uint32_t at = base + (uint32_t)__popc(mask & ((1u << lane) - 1u));
+    const uint64_t key = cand_key(score, s);
+    if (at < (uint32_t)CAP) {
+      stage[jb * CAP + at] = key;
+    } else {
+      const int g = atomicAdd(cnt + slot, 1);
+      if (g < C) cand[(size_t)slot * C + g] = key;
+    }
   }
+}
+
+// Move one item's staged candidates to the global buffers: warp w flushes
+// query slots w, w + kEpiWarps, ... and clears their staging counters.
+template <int QB, int CAP>
+__device__ __forceinline__ void flush_staged(int block, uint32_t* scnt, const uint64_t* stage,
+                                             int32_t* cnt, uint64_t* cand, int C, int ewarp) {
+  const int lane = threadIdx.x & 31;
+  for (int jb = ewarp; jb < QB; jb += kEpiWarps) {
+    const uint32_t n = min(scnt[jb], (uint32_t)CAP);
+    if (n == 0) continue;
+    const int slot = block * QB + jb;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(cnt + slot, (int)n);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    for (uint32_t i = lane; i < n; i += 32) {
+      const int g = base + (int)i;
+      if (g < C) cand[(size_t)slot * C + g] = stage[jb * CAP + i];
+    }
+  }
+  __syncwarp();
+  for (int jb = ewarp; jb < QB; jb += kEpiWarps)
+    if (lane == 0) scnt[jb] = 0;
 }
 
 template <int D, int DT, int H, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_stream(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
              const Args a) {
-  using C_ = Cfg<D, DT, H>;
+  using C_ = Cfg<D, DT, H, MODE == 0 ? 1 : 0>;
   using Geo = typename C_::Geo;
   constexpr int G = C_::G, NG = C_::NG, QB = C_::QB, STAGES = C_::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
@@ -201,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* pos_s = reinterpret_cast<int32_t*>(smem + C_::POS_OFF);
   float* thr_s = reinterpret_cast<float*>(smem + C_::THR_OFF);
   int32_t* row_s = reinterpret_cast<int32_t*>(smem + C_::ROW_OFF);
+  uint32_t* scnt_s = reinterpret_cast<uint32_t*>(smem + C_::SCNT_OFF);
+  uint64_t* stage_s = reinterpret_cast<uint64_t*>(smem + C_::STAGE_OFF);
+  constexpr int CAP = C_::STAGE_CAP;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (a.L + kChunkKeys - 1) / kChunkKeys;
@@ -348,9 +389,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 128;
     int acc = 0;
     uint32_t aphase = 0;
+    int prev_block = -1;
+    if (MODE == 0)
+      for (int jb = et; jb < QB; jb += kEpiWarps * 32) scnt_s[jb] = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
       const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
       epi_sync();
+      if (MODE == 0 && prev_block >= 0)
+        flush_staged<QB, CAP>(prev_block, scnt_s, stage_s, a.cnt, a.cand, a.C, e);
+      prev_block = itm.block;
       for (int j = et; j < QB * H; j += kEpiWarps * 32) {
         const int jb = j / H, h = j % H;
         float wv;
@@ -405,32 +452,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_after_sync();
           const uint32_t tbase =
               tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + sub * CW);
-          // this warp's CW columns = queries qlo .. of group g (whole queries: CW % H == 0)
+          // this warp's CW columns = queries qlo .. of group g (whole queries: CW % H == 0);
+          // per-warp base pointers so that every shared load below has a constant offset
           const int qlo = g * G + (sub * CW) / H;
+          const float* wrow = wq_s + qlo * H;  // weight of column c is wrow[c]
+          const int32_t* prow = pos_s + qlo;
+          const float* trow = thr_s + qlo;
+          const int32_t* rrow = row_s + qlo;
           HeadSum<H> hs;
           hs.reset();
+          float v[32];
+          tc::tmem_ld32(tbase, v);
+          tc::tmem_wait_ld(v);
 #pragma unroll
           for (int ch = 0; ch < CW / 32; ++ch) {
-            float v[32];
-            tc::tmem_ld32(tbase + ch * 32, v);
-            tc::tmem_wait_ld(v);
+            if (ch > 0) {
+              tc::tmem_ld32(tbase + ch * 32, v);
+              tc::tmem_wait_ld(v);
+            }
             constexpr int STEP = H == 1 ? 1 : (H == 2 ? 2 : 4);
 #pragma unroll
             for (int j = 0; j < 32; j += STEP) {
-              const int col = ch * 32 + j;       // column within this warp's span
-              const int jb = qlo + col / H;      // query slot within the block
+              const int col = ch * 32 + j;  // column within this warp's span
+              const int qi = col / H;       // query within the span
               const int h = col % H;
               float sc = 0.0f;
               bool done = false;
               if (H == 1) {
-                sc = single_head_score<H>(v[j], wq_s[jb]);
+                sc = single_head_score<H>(v[j], wrow[col]);
                 done = true;
               } else if (H == 2) {
-                const float2 w2 = *reinterpret_cast<const float2*>(wq_s + jb * H + h);
+                const float2 w2 = *reinterpret_cast<const float2*>(wrow + col);
                 hs.add_pair(h, v[j], v[j + 1], w2.x, w2.y);
                 done = true;
               } else {
-                const float4 w4 = *reinterpret_cast<const float4*>(wq_s + jb * H + h);
+                const float4 w4 = *reinterpret_cast<const float4*>(wrow + col);
                 hs.add_pair(h, v[j], v[j + 1], w4.x, w4.y);
                 hs.add_pair(h + 2, v[j + 2], v[j + 3], w4.z, w4.w);
                 done = (h + 4 == H);
@@ -441,12 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                   hs.reset();
                 }
                 sc = finish_score(sc, ks);
-                const int p = pos_s[jb];
+                const int p = prow[qi];
                 if (MODE == 0) {
-                  const bool pass = (s <= p) && (sc >= thr_s[jb]);
-                  append(pass, sc, s, row_s[jb], a.cnt, a.cand, a.C);
+                  const bool pass = (s <= p) && (sc >= trow[qi]);
+                  append_staged<CAP>(pass, sc, s, qlo + qi, rrow[qi], scnt_s, stage_s, a.cnt,
+                                     a.cand, a.C);
                 } else {
-                  const int r = row_s[jb];
+                  const int r = rrow[qi];
                   if (r >= 0 && s < a.L)
                     a.table[(size_t)r * a.L + s] = (s <= p) ? sc : -__int_as_float(0x7f800000);
                 }
@@ -460,6 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (acc == 0) aphase ^= 1u;
         }
       }
+    }
+    if (MODE == 0) {
+      epi_sync();
+      if (prev_block >= 0)
+        flush_staged<QB, CAP>(prev_block, scnt_s, stage_s, a.cnt, a.cand, a.C, e);
     }
   }
   tc::fence_before_sync();
