@@ -84,7 +84,7 @@ struct GArgs {
 };
 
 template <int D, int DT, int H, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) k_gather(const GArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   using C_ = Cfg<D, DT, H, MODE>;
   using Geo = typename C_::Geo;
   constexpr int NQ = C_::NQ, STAGES = C_::STAGES, CPR = C_::CPR, RB = C_::RB;
@@ -295,22 +295,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gather(const GArgs a) {
         stream::HeadSum<H> hs;
         hs.reset();
         float sc;
-        if (H >= 64) {
+        if (H >= 32) {
 #pragma unroll
-          for (int c0 = 0; c0 < H; c0 += 64) {
-            float v[64];
-            tc::tmem_ld64(taddr + c0, v);
+          for (int c0 = 0; c0 < H; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32(taddr + c0, v);
             tc::tmem_wait_ld(v);
 #pragma unroll
-            for (int h = 0; h < 64; h += 2) hs.add_pair(c0 + h, v[h], v[h + 1], wq_s[c0 + h], wq_s[c0 + h + 1]);
+            for (int h = 0; h < 32; h += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wq_s + c0 + h);
+              hs.add_pair(c0 + h, v[h], v[h + 1], w4.x, w4.y);
+              hs.add_pair(c0 + h + 2, v[h + 2], v[h + 3], w4.z, w4.w);
+            }
           }
-          sc = hs.total();
-        } else if (H == 32) {
-          float v[32];
-          tc::tmem_ld32(taddr, v);
-          tc::tmem_wait_ld(v);
-#pragma unroll
-          for (int h = 0; h < 32; h += 2) hs.add_pair(h, v[h], v[h + 1], wq_s[h], wq_s[h + 1]);
           sc = hs.total();
         } else {
           float v[16];

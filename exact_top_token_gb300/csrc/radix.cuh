@@ -57,6 +57,17 @@ __device__ __forceinline__ void cta_find_crossing(const uint32_t* hist, int nbin
   __syncthreads();
 }
 
+// Warp-aggregated histogram increment: lanes of a warp that hit the same bin
+// add their count with one shared atomic (scores of a query share their top
+// bits, so without aggregation most increments collide on a few bins). All 32
+// lanes must call it; `active` lanes contribute.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
+  const unsigned act = __ballot_sync(0xffffffffu, active);
+  if (!active) return;
+  const unsigned peers = __match_any_sync(act, bin);
+  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+}
+
 // Shared-memory scratch of the selection helpers.
 struct alignas(16) RadixScratch {
   uint32_t hist[4096];
@@ -73,9 +84,11 @@ static __device__ uint32_t cta_kth_smallest_u32(const uint32_t* keys, int cnt, u
     const int shift = 24 - pbits;
     for (int b = threadIdx.x; b < 256; b += blockDim.x) sc.hist[b] = 0;
     __syncthreads();
-    for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-      const uint32_t key = keys[e];
-      if (pbits == 0 || (key >> (32 - pbits)) == prefix) atomicAdd(&sc.hist[(key >> shift) & 255u], 1u);
+    for (int e0 = 0; e0 < cnt; e0 += blockDim.x) {
+      const int e = e0 + threadIdx.x;
+      const uint32_t key = e < cnt ? keys[e] : 0u;
+      const bool in = e < cnt && (pbits == 0 || (key >> (32 - pbits)) == prefix);
+      hist_add(sc.hist, (key >> shift) & 255u, in);
     }
     __syncthreads();
     cta_find_crossing(sc.hist, 256, kk, sc.warp_sums, sc.out);
@@ -103,10 +116,11 @@ static __device__ int cta_select_smallest_u64(const uint64_t* list, int cnt, int
     const int shift = 56 - pbits;
     for (int b = threadIdx.x; b < 256; b += blockDim.x) sc.hist[b] = 0;
     __syncthreads();
-    for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-      const uint64_t key = list[e];
-      if (pbits == 0 || (key >> (64 - pbits)) == prefix)
-        atomicAdd(&sc.hist[(uint32_t)(key >> shift) & 255u], 1u);
+    for (int e0 = 0; e0 < cnt; e0 += blockDim.x) {
+      const int e = e0 + threadIdx.x;
+      const uint64_t key = e < cnt ? list[e] : 0ull;
+      const bool in = e < cnt && (pbits == 0 || (key >> (64 - pbits)) == prefix);
+      hist_add(sc.hist, (uint32_t)(key >> shift) & 255u, in);
     }
     __syncthreads();
     cta_find_crossing(sc.hist, 256, krem, sc.warp_sums, sc.out);
@@ -181,7 +195,10 @@ static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_
   if (k_eff <= 0) return 0;
   for (int b = threadIdx.x; b < 4096; b += blockDim.x) sc.hist[b] = 0;
   __syncthreads();
-  for (int s = threadIdx.x; s < ctx; s += blockDim.x) atomicAdd(&sc.hist[desc32(row[s]) >> 20], 1u);
+  for (int s0 = 0; s0 < ctx; s0 += blockDim.x) {
+    const int s = s0 + threadIdx.x;
+    hist_add(sc.hist, s < ctx ? desc32(row[s]) >> 20 : 0u, s < ctx);
+  }
   __syncthreads();
   cta_find_crossing(sc.hist, 4096, (uint32_t)k_eff, sc.warp_sums, sc.out);
   const uint32_t bin = sc.out[0];
