@@ -183,6 +183,20 @@ __device__ __forceinline__ int sample_position(int64_t ctx, int m, int j) {
   return (int)(((int64_t)j * ctx) / m);
 }
 
+// p_j = floor(j * ctx / M) without 64-bit division: with ctx = a*M + b,
+// p_j = j*a + floor(j*b / M), and j*b < M^2 <= 2^26 fits 32 bits.
+struct SampleStep {
+  uint32_t a, b, m;
+  __device__ __forceinline__ void init(int64_t ctx, int M) {
+    m = (uint32_t)M;
+    a = (uint32_t)(ctx / M);
+    b = (uint32_t)(ctx - (int64_t)a * M);
+  }
+  __device__ __forceinline__ int at(int j) const {
+    return (int)((uint32_t)j * a + ((uint32_t)j * b) / m);
+  }
+};
+
 // Entries of the shared-memory sort buffer for k keys: the next power of two,
 // at least 2 (so that what follows it stays 16-byte aligned).
 __host__ __device__ __forceinline__ int sort_capacity(int k) {

@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
     }
     if (*abort_flag) break;
     int slot = -1, t = -1, ctx = 0, nrows = 0, M = 0, r = 0;
+    SampleStep step{};
     if (MODE == kReplay) {
       t = item;
       nrows = a.k_top;
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
         }
         M = sample_count(ctx);
         r = threshold_rank(ctx, a.k_top, M);
+        step.init(ctx, M);
         nrows = M;
       } else {
         nrows = ctx;
@@ -209,20 +211,24 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       for (int i = 0; i < ntiles; ++i) {
         if (!tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status)) break;
         uint8_t* dst = ring + p_stage * C_::KT_BYTES;
-        for (int f = tid; f < kTileKeys * CPR; f += kProducers) {
-          const int row = f / CPR, c = f % CPR;
+        {
+          // one row per producer thread: its key position, then its d bytes
+          const int row = tid;
           const int j = i * kTileKeys + row;
           int s = -1;
           if (j < nrows) {
-            if (MODE == kThreshold) s = sample_position(ctx, M, j);
+            if (MODE == kThreshold) s = step.at(j);
             else if (MODE == kReplay) {
               s = __ldg(a.idx + (size_t)t * a.k_top + j);
               if (s < 0 || s >= a.L) s = -1;
             } else s = j;
           }
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(a.k) +
-                               (s >= 0 ? (size_t)s * RB + c * 16 : 0);
-          tc::cp_async16(dst + Geo::chunk_offset(row, c, kTileKeys), src, s >= 0);
+          const uint8_t* src =
+              reinterpret_cast<const uint8_t*>(a.k) + (s >= 0 ? (size_t)s * RB : 0);
+#pragma unroll
+          for (int c = 0; c < CPR; ++c)
+            tc::cp_async16(dst + Geo::chunk_offset(row, c, kTileKeys), src + (s >= 0 ? c * 16 : 0),
+                           s >= 0);
         }
         tc::cp_async_commit();
         ++npend;
@@ -286,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
         const int j = i * kTileKeys + row;
         int s = -1;
         if (j < nrows) {
-          if (MODE == kThreshold) s = sample_position(ctx, M, j);
+          if (MODE == kThreshold) s = step.at(j);
           else if (MODE == kReplay) s = __ldg(a.idx + (size_t)t * a.k_top + j);
           else s = j;
         }
