@@ -16,9 +16,9 @@
 // The CTA then finishes the query together: the r-th best sample (threshold),
 // nothing (replay), or an exact top-k of the rescored row (recovery).
 //
-//   warps 0..1  producers (cp.async gather, 64 threads, two key rows each)
-//   warp 2      MMA issuer and TMEM allocator; warp 3 idle
-//   warps 4..7  epilogue
+//   warps 0..3  producers (cp.async gather, 128 threads)
+//   warp 4      MMA issuer; warp 5 TMEM allocator
+//   warps 8..11 epilogue
 #pragma once
 
 #include "radix.cuh"
@@ -27,10 +27,9 @@
 namespace hytopk {
 namespace gather {
 
-constexpr int kThreads = 256;
-constexpr int kProducers = 64;   // warps 0..1, two key rows per thread
-constexpr int kMmaWarp = 2;      // also owns the TMEM allocation
-constexpr int kEpiFirstWarp = 4;
+constexpr int kThreads = 384;
+constexpr int kProducers = 128;
+constexpr int kEpiFirstWarp = 8;
 constexpr int kSlots = 2;  // TMEM accumulators
 
 enum Mode { kThreshold = 0, kReplay = 1, kRecover = 2 };
@@ -85,7 +84,7 @@ struct GArgs {
 };
 
 template <int D, int DT, int H, int MODE>
-__global__ void __launch_bounds__(kThreads, 3) k_gather(const GArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   using C_ = Cfg<D, DT, H, MODE>;
   using Geo = typename C_::Geo;
   constexpr int NQ = C_::NQ, STAGES = C_::STAGES, CPR = C_::CPR, RB = C_::RB;
@@ -122,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_gather(const GArgs a) {
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == 5) {
     tc::tmem_alloc(tmem_slot, C_::TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -205,17 +204,16 @@ __global__ void __launch_bounds__(kThreads, 3) k_gather(const GArgs a) {
       __syncthreads();
     }
 
-    if (warp < kProducers / 32) {
+    if (warp < 4) {
       // ---------------- producers: gather 128 key rows per tile ----------------
       const int tid = threadIdx.x;
       int npend = 0;
       for (int i = 0; i < ntiles; ++i) {
         if (!tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status)) break;
         uint8_t* dst = ring + p_stage * C_::KT_BYTES;
-#pragma unroll
-        for (int rr = 0; rr < kTileKeys / kProducers; ++rr) {
-          // rows tid, tid + 64: the key position, then its d bytes
-          const int row = tid + rr * kProducers;
+        {
+          // one row per producer thread: its key position, then its d bytes
+          const int row = tid;
           const int j = i * kTileKeys + row;
           int s = -1;
           if (j < nrows) {
@@ -249,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_gather(const GArgs a) {
       tc::cp_async_wait<0>();
       tc::fence_proxy_async_smem();
       for (; npend > 0; --npend) tc::mbar_arrive(full + (p_stage - npend + STAGES) % STAGES);
-    } else if (warp == kMmaWarp) {
+    } else if (warp == 4) {
       if (lane == 0) {
         // ---------------- MMA issuer ----------------
         constexpr uint32_t IDESC = tc::instr_desc(DT, 128, NQ);
@@ -375,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_gather(const GArgs a) {
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == 5) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, C_::TMEM_COLS);
   }
