@@ -9,17 +9,16 @@
 // (rescore only the k stored entries).
 //
 // Per query: the key rows it needs (samples, stored indices or its whole
-// prefix) are gathered 128 at a time by TMA (tile::gather4: four arbitrary
-// rows per instruction, one instruction per producer lane and swizzle atom)
-// into swizzled shared memory; one elected thread multiplies each tile by the query's
+// prefix) are gathered 128 at a time with cp.async into swizzled shared
+// memory; one elected thread multiplies each 128-key tile by the query's
 // H x d operand (tcgen05, N = max(H, 16)); four epilogue warps (TMEM lane =
 // key) reduce the heads with the same arithmetic as the streaming engine.
 // The CTA then finishes the query together: the r-th best sample (threshold),
 // nothing (replay), or an exact top-k of the rescored row (recovery).
 //
-//   warp 0      producer (TMA gathers, 4 rows per lane)
-//   warp 1      MMA issuer and TMEM allocator; warps 2..3 idle
-//   warps 4..7  epilogue
+//   warps 0..3  producers (cp.async gather, 128 threads)
+//   warp 4      MMA issuer; warp 5 TMEM allocator
+//   warps 8..11 epilogue
 #pragma once
 
 #include "radix.cuh"
@@ -28,9 +27,9 @@
 namespace hytopk {
 namespace gather {
 
-constexpr int kThreads = 256;
-constexpr int kMmaWarp = 1;
-constexpr int kEpiFirstWarp = 4;
+constexpr int kThreads = 384;
+constexpr int kProducers = 128;
+constexpr int kEpiFirstWarp = 8;
 constexpr int kSlots = 2;  // TMEM accumulators
 
 enum Mode { kThreshold = 0, kReplay = 1, kRecover = 2 };
@@ -85,8 +84,7 @@ struct GArgs {
 };
 
 template <int D, int DT, int H, int MODE>
-__global__ void __launch_bounds__(kThreads, 3)
-    k_gather(const __grid_constant__ CUtensorMap kmap, const GArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   using C_ = Cfg<D, DT, H, MODE>;
   using Geo = typename C_::Geo;
   constexpr int NQ = C_::NQ, STAGES = C_::STAGES, CPR = C_::CPR, RB = C_::RB;
@@ -113,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      tc::mbar_init(full + i, 1);
+      tc::mbar_init(full + i, kProducers);
       tc::mbar_init(empty + i, 1);
     }
     for (int i = 0; i < kSlots; ++i) {
@@ -123,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == 5) {
     tc::tmem_alloc(tmem_slot, C_::TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -206,19 +204,17 @@ __global__ void __launch_bounds__(kThreads, 3)
       __syncthreads();
     }
 
-    if (warp == 0) {
-      // ---------------- producer: TMA gathers of 128 key rows per tile ----------------
-      uint32_t pending = 0, pend_phase = 0;  // issued loads, for a clean abort
+    if (warp < 4) {
+      // ---------------- producers: gather 128 key rows per tile ----------------
+      const int tid = threadIdx.x;
+      int npend = 0;
       for (int i = 0; i < ntiles; ++i) {
-        int ok = 1;
-        if (lane == 0) ok = tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (lane == 0) tc::mbar_expect_tx(full + p_stage, C_::KT_BYTES);
-        __syncwarp();
-        int rows[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = i * kTileKeys + lane * 4 + u;
+        if (!tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status)) break;
+        uint8_t* dst = ring + p_stage * C_::KT_BYTES;
+        {
+          // one row per producer thread: its key position, then its d bytes
+          const int row = tid;
+          const int j = i * kTileKeys + row;
           int s = -1;
           if (j < nrows) {
             if (MODE == kThreshold) s = step.at(j);
@@ -227,31 +223,31 @@ __global__ void __launch_bounds__(kThreads, 3)
               if (s < 0 || s >= a.L) s = -1;
             } else s = j;
           }
-          rows[u] = s >= 0 ? s : 0;  // rows that are not needed load key 0 (ignored)
-        }
-        uint8_t* dst = ring + p_stage * C_::KT_BYTES;
+          const uint8_t* src =
+              reinterpret_cast<const uint8_t*>(a.k) + (s >= 0 ? (size_t)s * RB : 0);
 #pragma unroll
-        for (int at = 0; at < Geo::kAtoms; ++at)
-          tc::tma_gather4(dst + at * kTileKeys * Geo::kAtom + lane * 4 * Geo::kAtom, &kmap,
-                          full + p_stage, at * Geo::kAtom / C_::ES, rows[0], rows[1], rows[2],
-                          rows[3]);
-        pending |= 1u << p_stage;
-        pend_phase = (pend_phase & ~(1u << p_stage)) | (p_phase << p_stage);
+          for (int c = 0; c < CPR; ++c)
+            tc::cp_async16(dst + Geo::chunk_offset(row, c, kTileKeys), src + (s >= 0 ? c * 16 : 0),
+                           s >= 0);
+        }
+        tc::cp_async_commit();
+        ++npend;
+        if (npend == STAGES - 1) {
+          tc::cp_async_wait<STAGES - 2>();
+          tc::fence_proxy_async_smem();
+          const int st = (p_stage - (npend - 1) + STAGES) % STAGES;
+          tc::mbar_arrive(full + st);
+          --npend;
+        }
         if (++p_stage == STAGES) {
           p_stage = 0;
           p_phase ^= 1u;
         }
       }
-      if (*abort_flag && lane == 0) {
-        // let the copies still in flight land before the CTA moves on (bounded)
-        const uint64_t t0 = tc::global_ns();
-        for (int st = 0; st < STAGES; ++st)
-          if (pending & (1u << st))
-            while (!tc::mbar_try_wait(full + st, (pend_phase >> st) & 1u) &&
-                   tc::global_ns() - t0 < 200000000ull) {
-            }
-      }
-    } else if (warp == kMmaWarp) {
+      tc::cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      for (; npend > 0; --npend) tc::mbar_arrive(full + (p_stage - npend + STAGES) % STAGES);
+    } else if (warp == 4) {
       if (lane == 0) {
         // ---------------- MMA issuer ----------------
         constexpr uint32_t IDESC = tc::instr_desc(DT, 128, NQ);
@@ -377,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == 5) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, C_::TMEM_COLS);
   }

@@ -5,37 +5,25 @@
 
 namespace hytopk {
 
-cudaError_t launch_gather_d64_bf16(int H, int mode, const CUtensorMap& km,
-                                    const gather::GArgs& a, int items,
+cudaError_t launch_gather_d64_bf16(int H, int mode, const gather::GArgs& a, int grid,
                                    cudaStream_t st);
-cudaError_t launch_gather_d64_e4m3(int H, int mode, const CUtensorMap& km,
-                                    const gather::GArgs& a, int items,
+cudaError_t launch_gather_d64_e4m3(int H, int mode, const gather::GArgs& a, int grid,
                                    cudaStream_t st);
-cudaError_t launch_gather_d128_bf16(int H, int mode, const CUtensorMap& km,
-                                    const gather::GArgs& a, int items,
+cudaError_t launch_gather_d128_bf16(int H, int mode, const gather::GArgs& a, int grid,
                                     cudaStream_t st);
-cudaError_t launch_gather_d128_e4m3(int H, int mode, const CUtensorMap& km,
-                                    const gather::GArgs& a, int items,
+cudaError_t launch_gather_d128_e4m3(int H, int mode, const gather::GArgs& a, int grid,
                                     cudaStream_t st);
 
 namespace {
 
-// Tensor map of the keys for TMA gathers: boxes one row high, one swizzle atom
-// (128 or 64 bytes) wide.
-cudaError_t dispatch(const Problem& p, int mode, const gather::GArgs& a, int items,
+cudaError_t dispatch(const Problem& p, int mode, const gather::GArgs& a, int grid,
                      cudaStream_t st) {
-  if (items <= 0) return cudaSuccess;
-  const int rb = p.d * (p.dt == 0 ? 2 : 1);
-  const int atom = rb >= 128 ? 128 : 64;
-  CUtensorMap km;
-  if (!make_tmap_2d(&km, p.k, p.dt, (uint64_t)p.d, (uint64_t)p.L, atom / (p.dt == 0 ? 2 : 1), 1,
-                    atom))
-    return cudaErrorInvalidValue;
+  if (grid <= 0) return cudaSuccess;
   if (p.d == 64)
-    return p.dt == 0 ? launch_gather_d64_bf16(p.H, mode, km, a, items, st)
-                     : launch_gather_d64_e4m3(p.H, mode, km, a, items, st);
-  return p.dt == 0 ? launch_gather_d128_bf16(p.H, mode, km, a, items, st)
-                   : launch_gather_d128_e4m3(p.H, mode, km, a, items, st);
+    return p.dt == 0 ? launch_gather_d64_bf16(p.H, mode, a, grid, st)
+                     : launch_gather_d64_e4m3(p.H, mode, a, grid, st);
+  return p.dt == 0 ? launch_gather_d128_bf16(p.H, mode, a, grid, st)
+                   : launch_gather_d128_e4m3(p.H, mode, a, grid, st);
 }
 
 gather::GArgs base_args(const Problem& p) {
@@ -62,6 +50,11 @@ void slot_args(gather::GArgs& a, const SelectWs& ws) {
   a.status = ws.counters + kCtrStatus;
 }
 
+int capped_grid(int items) {
+  const int g = 2 * num_sms();
+  return items < g ? items : g;
+}
+
 }  // namespace
 
 cudaError_t launch_threshold(const Problem& p, const SelectWs& ws, const float* override_thr,
@@ -69,7 +62,7 @@ cudaError_t launch_threshold(const Problem& p, const SelectWs& ws, const float* 
   gather::GArgs a = base_args(p);
   slot_args(a, ws);
   a.override_thr = override_thr;
-  return dispatch(p, gather::kThreshold, a, ws.n_pad, st);
+  return dispatch(p, gather::kThreshold, a, capped_grid(ws.n_pad), st);
 }
 
 cudaError_t launch_recover(const Problem& p, const SelectWs& ws, int32_t* idx_out,
@@ -90,7 +83,7 @@ cudaError_t launch_replay(const Problem& p, const int32_t* idx, float* out, uint
   a.idx = idx;
   a.out = out;
   a.status = status;
-  return dispatch(p, gather::kReplay, a, p.n, st);
+  return dispatch(p, gather::kReplay, a, capped_grid(p.n), st);
 }
 
 }  // namespace hytopk

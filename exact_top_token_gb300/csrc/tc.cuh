@@ -103,18 +103,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Four arbitrary rows (y0..y3) of a 2D tensor, columns [x, x + box), into four
-// consecutive rows at dst with the tensor map's swizzle; completes on bar.
-// The tensor map's box must be one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int x, int y0, int y1, int y2, int y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // ---- cp.async (gathered rows) ---------------------------------------------------------
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
