@@ -43,6 +43,10 @@ REPLAY_BYTES_PER_ENTRY = {  # idx 4 + key row d*esize + key scale + out 4 + q/w 
     "e4m3": 4 + 128 + 4 + 4 + 4.25, "bf16": 4 + 256 + 4 + 4.25}
 WORKLOADS = {"glm_1m": si.glm_1m, "mixed_contexts": si.mixed_contexts,
              "tiny_exact": si.tiny_exact}
+# DRAM bytes (read + write) of one full-size filter launch, from the ncu
+# capture summarised in profiles/glm_1m_launch_list_tensorcore.txt. Must be
+# re-captured (or set to None) whenever the filter kernel changes.
+FILTER_TRAFFIC_BYTES = {"glm_1m": 1.4409e9 + 0.4032e9}
 
 
 def parse():
@@ -304,7 +308,9 @@ def gpu_arm(args, world, rank, local):
     peak = pk["bf16_tflops"] * (2.0 if case["dtype"] == "e4m3" else 1.0)
     roofline = {"kernel": "k_stream filter (fused score + threshold filter)", "bound": "tensor",
                 "achieved": achieved_tflops, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved_tflops / peak, "traffic": None,
+                "frac": achieved_tflops / peak,
+                "traffic": (None if args.queries else FILTER_TRAFFIC_BYTES.get(args.workload)),
+                "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "algorithmic_flops_per_launch": pairs * flops_per_pair,
                 "peak_source": (f"{'2 x ' if case['dtype'] == 'e4m3' else ''}measured bf16 burst "
                                 f"{pk['bf16_tflops']} TFLOP/s ({pk['source']})")}
