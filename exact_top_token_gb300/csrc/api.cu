@@ -205,15 +205,22 @@ hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
   return HYTOPK_OK;
 }
 
-static size_t twopass_fixed_bytes(int L) {
-  return align_up((size_t)kRecoveryCtas * L * 8, 1024);
+// Two-pass workspace: the per-CTA candidate lists of the read-back kernel, the
+// halved folded weights of the queries (padded by one query block), then the
+// score-table chunk.
+static size_t twopass_lists_bytes(int L) { return align_up((size_t)kRecoveryCtas * L * 8, 1024); }
+static size_t twopass_weights_bytes(int n, int H) {
+  return align_up(((size_t)n + kQueryPad) * H * 4, 1024);
+}
+static size_t twopass_fixed_bytes(int n, int L, int H) {
+  return twopass_lists_bytes(L) + twopass_weights_bytes(n, H);
 }
 
 size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,
                                      int rows_per_chunk) {
   if (check_shape(n, L, H, d, k_top, dt) != HYTOPK_OK) return 0;
   const int rows = rows_per_chunk <= 0 ? (n > 0 ? n : 1) : rows_per_chunk;
-  return twopass_fixed_bytes(L) + align_up((size_t)rows * L * 4, 1024);
+  return twopass_fixed_bytes(n, L, H) + align_up((size_t)rows * L * 4, 1024);
 }
 
 hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const void* k,
@@ -229,18 +236,20 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
   if (n == 0) return HYTOPK_OK;
   if (!positions || !idx_out || !workspace) return HYTOPK_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HYTOPK_MISALIGNED;
-  const size_t fixed = twopass_fixed_bytes(L);
+  const size_t fixed = twopass_fixed_bytes(n, L, H);
   const size_t row_bytes = (size_t)L * 4;
   if (workspace_bytes < fixed + row_bytes) return HYTOPK_WORKSPACE_TOO_SMALL;
   size_t chunk = (workspace_bytes - fixed) / row_bytes;
   if (chunk > (size_t)n) chunk = (size_t)n;
   uint8_t* base = static_cast<uint8_t*>(workspace);
   uint64_t* lists = reinterpret_cast<uint64_t*>(base);
+  float* hw = reinterpret_cast<float*>(base + twopass_lists_bytes(L));
   float* table = reinterpret_cast<float*>(base + fixed);
   const Problem p = make_problem(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt);
+  HYTOPK_TRY(launch_fold_weights(p, n + kQueryPad, hw, stream));
   for (int row0 = 0; row0 < n; row0 += (int)chunk) {
     const int rows = (int)((size_t)(n - row0) < chunk ? (size_t)(n - row0) : chunk);
-    HYTOPK_TRY(launch_table(p, row0, rows, table, dev_status, stream));
+    HYTOPK_TRY(launch_table(p, row0, rows, table, hw, dev_status, stream));
     HYTOPK_TRY(launch_table_topk(p, row0, rows, table, lists, kRecoveryCtas, idx_out, scores_out,
                                  stream));
   }

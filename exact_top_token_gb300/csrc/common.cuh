@@ -55,7 +55,7 @@ struct Problem {
 struct SelectWs {
   int32_t* perm;        // [n_pad] slot -> query index, -1 for padding
   int32_t* qpos;        // [n_pad] slot -> position, -1 for padding / bad position
-  float* wq;            // [n_pad, H] folded head weights
+  float* wq;            // [n_pad, H] folded, halved head weights w * q_scale / 2
   void* qp;             // [n_pad, H, d] packed query elements
   float* thr;           // [n_pad] thresholds
   int32_t* cnt;         // [n_pad] candidate counts (may exceed C: overflow)
@@ -119,29 +119,6 @@ __device__ __forceinline__ float load_elem(const void* base, size_t i) {
 __device__ __forceinline__ float finish_score(float acc, float ks) {
   float s = acc * ks;
   return s == 0.0f ? 0.0f : s;
-}
-
-// Score of one key (raw row in registers) for one query whose raw q rows
-// [H][D] and folded weights [H] sit in shared memory.
-template <int D>
-__device__ __forceinline__ float score_key_simt(const float* __restrict__ qf,
-                                                const float* __restrict__ wq, int H,
-                                                const float (&kr)[D], float ks) {
-  float acc = 0.0f;
-  for (int h = 0; h < H; ++h) {
-    const float4* q4 = reinterpret_cast<const float4*>(qf + h * D);
-    float dot = 0.0f;
-#pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-      float4 v = q4[i];
-      dot = fmaf(v.x, kr[4 * i + 0], dot);
-      dot = fmaf(v.y, kr[4 * i + 1], dot);
-      dot = fmaf(v.z, kr[4 * i + 2], dot);
-      dot = fmaf(v.w, kr[4 * i + 3], dot);
-    }
-    acc = fmaf(wq[h], fmaxf(dot, 0.0f), acc);
-  }
-  return finish_score(acc, ks);
 }
 
 // ---- ordered keys -------------------------------------------------------------------

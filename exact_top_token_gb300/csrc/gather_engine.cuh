@@ -191,14 +191,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
         *reinterpret_cast<uint4*>(qbuf + Geo::chunk_offset(row, c, NQ)) = v;
       }
       for (int h = threadIdx.x; h < H; h += kThreads) {
-        float wv;
+        float hw;  // halved folded weight, as in the prep kernel
         if (MODE == kReplay) {
-          wv = a.w[(size_t)t * H + h];
+          float wv = a.w[(size_t)t * H + h];
           if (DT == 1) wv *= a.q_scale[(size_t)t * H + h];
+          hw = 0.5f * wv;
         } else {
-          wv = a.wq[(size_t)slot * H + h];
+          hw = a.wq[(size_t)slot * H + h];
         }
-        wq_s[h] = 0.5f * wv;  // halved: see stream::HeadSum
+        wq_s[h] = hw;
       }
       tc::fence_proxy_async_smem();
       __syncthreads();

@@ -11,6 +11,7 @@ namespace hytopk {
 
 // prep.cu
 cudaError_t launch_prep(const Problem& p, const SelectWs& ws, cudaStream_t st);
+cudaError_t launch_fold_weights(const Problem& p, int rows, float* hw, cudaStream_t st);
 
 // score_*.cu: the scoring phases
 cudaError_t launch_threshold(const Problem& p, const SelectWs& ws, const float* override_thr,
@@ -20,8 +21,8 @@ cudaError_t launch_recover(const Problem& p, const SelectWs& ws, int32_t* idx_ou
                            float* scores_out, cudaStream_t st);
 cudaError_t launch_replay(const Problem& p, const int32_t* idx, float* out, uint32_t* status,
                           cudaStream_t st);
-cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, uint32_t* status,
-                         cudaStream_t st);
+cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, const float* hw,
+                         uint32_t* status, cudaStream_t st);
 
 // select.cu
 cudaError_t launch_check(const Problem& p, const SelectWs& ws, cudaStream_t st);

@@ -5,9 +5,10 @@
 // so that a block of adjacent slots has nearly equal causal ranges (little
 // masked work in a shared key tile) and the longest blocks are scheduled
 // first. Packing copies each query's q rows to its slot, folds the fp8 query
-// scale into the head weight (wq = w * q_scale, valid because scales are
-// positive) and records the position. Slots past n are padding with
-// position -1 (no keys).
+// scale into the head weight and halves it (hw = w * q_scale / 2, valid
+// because scales are positive; the halving is exact and is undone by the
+// ReLU form (x + |x|) * hw of the epilogue), and records the position. Slots
+// past n are padding with position -1 (no keys).
 #include <climits>
 
 #include "launch.h"
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(128) k_pack_queries(Problem p, SelectWs ws) {
       if (!(qs > 0.0f)) set_status(ws.counters, HYTOPK_DEV_BAD_SCALE);
       wv *= qs;
     }
-    ws.wq[(size_t)slot * p.H + h] = wv;
+    ws.wq[(size_t)slot * p.H + h] = 0.5f * wv;
   }
   if (threadIdx.x == 0) {
     const int pos = clean_position(p.positions, t, p.L);
@@ -86,7 +87,28 @@ __global__ void k_check_key_scales(const float* __restrict__ k_scale, int L, uin
   if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(counters, HYTOPK_DEV_BAD_SCALE);
 }
 
+// Halved folded weights of the original queries (two-pass path): rows n..rows-1
+// are zero padding.
+__global__ void k_fold_weights(Problem p, int rows, float* __restrict__ hw) {
+  const size_t total = (size_t)rows * p.H;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = i / p.H;
+    float wv = 0.0f;
+    if (t < (size_t)p.n) {
+      wv = p.w[i];
+      if (p.dt == 1) wv *= p.q_scale[i];
+    }
+    hw[i] = 0.5f * wv;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fold_weights(const Problem& p, int rows, float* hw, cudaStream_t st) {
+  k_fold_weights<<<256, 256, 0, st>>>(p, rows, hw);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prep(const Problem& p, const SelectWs& ws, cudaStream_t st) {
   if (p.n > 0) k_rank_by_position<<<(p.n + 1023) / 1024, 1024, 0, st>>>(p.positions, p.n, p.L, ws.perm);

@@ -29,7 +29,9 @@ namespace stream {
 
 constexpr int kChunkTiles = 64;
 constexpr int kChunkKeys = kChunkTiles * kTileKeys;
-constexpr int kEpiWarps = 16;
+constexpr int kEpiWarps = 16;   // epilogue warps (4 per TMEM lane quadrant)
+constexpr int kChunk = 32;      // TMEM columns per tcgen05.ld in the epilogue
+constexpr bool kLookahead = false;  // load chunk c+1 while reducing chunk c
 constexpr int kThreads = 128 + kEpiWarps * 32;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (and its 512 TMEM columns) per SM
 
@@ -49,8 +51,7 @@ struct Cfg {
   static constexpr int BAR_OFF = K_OFF + STAGES * KT_BYTES;
   static constexpr int NBARS = 2 * STAGES + 4 + 2;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;      // tmem base, abort flag
-  static constexpr int WQ_OFF = MISC_OFF + 16;
-  static constexpr int POS_OFF = WQ_OFF + QB * H * 4;
+  static constexpr int POS_OFF = MISC_OFF + 16;
   static constexpr int THR_OFF = POS_OFF + QB * 4;
   static constexpr int ROW_OFF = THR_OFF + QB * 4;
   // per-item candidate staging (filter): CAP entries per query slot of the block
@@ -60,17 +61,19 @@ struct Cfg {
   static constexpr int END = STAGE_OFF + (MODE_STAGING ? QB * STAGE_CAP * 8 : 0);
   static constexpr int SMEM = (END + 1024) > kMinSmem ? (END + 1024) : kMinSmem;
   // epilogue: each warp owns one TMEM lane quadrant (32 keys) and CW columns
-  static constexpr int CW = H == 128 ? 128 : 64;
+  static constexpr int CW = H > (1024 / kEpiWarps) ? H : (1024 / kEpiWarps);
   static constexpr int ACTIVE_EPI = 4 * (256 / CW);  // warps that read accumulators
   static_assert(H >= 1 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two <= 128");
   static_assert(RB == 64 || RB == 128 || RB == 256, "row bytes");
 };
 
 struct Args {
+  // halved folded weights hw = w * q_scale / 2: [slots, H] (MODE 0) or
+  // [rows padded to the block size, H] (MODE 1)
+  const float* wq;
   // MODE 0 (filter): slots sorted by position; plan = chunk offsets
   const int32_t* qpos;
   const float* thr;
-  const float* wq;
   int32_t* cnt;
   uint64_t* cand;
   const int32_t* plan;  // [nchunks + 1] item offsets per key chunk
@@ -235,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_empty = bars + 2 * STAGES + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C_::MISC_OFF + 4);
-  float* wq_s = reinterpret_cast<float*>(smem + C_::WQ_OFF);
   int32_t* pos_s = reinterpret_cast<int32_t*>(smem + C_::POS_OFF);
   float* thr_s = reinterpret_cast<float*>(smem + C_::THR_OFF);
   int32_t* row_s = reinterpret_cast<int32_t*>(smem + C_::ROW_OFF);
@@ -398,22 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == 0 && prev_block >= 0)
         flush_staged<QB, CAP>(prev_block, scnt_s, stage_s, a.cnt, a.cand, a.C, e);
       prev_block = itm.block;
-      for (int j = et; j < QB * H; j += kEpiWarps * 32) {
-        const int jb = j / H, h = j % H;
-        float wv;
-        if (MODE == 0) {
-          wv = __ldg(a.wq + (size_t)(itm.block * QB + jb) * H + h);
-        } else {
-          const int r = itm.block * QB + jb;
-          const int t = a.row0 + r;
-          wv = 0.0f;
-          if (r < a.rows) {
-            wv = __ldg(a.w + (size_t)t * H + h);
-            if (DT == 1) wv *= __ldg(a.q_scale + (size_t)t * H + h);
-          }
-        }
-        wq_s[j] = 0.5f * wv;  // halved: see HeadSum
-      }
       for (int jb = et; jb < QB; jb += kEpiWarps * 32) {
         if (MODE == 0) {
           const int slot = itm.block * QB + jb;
@@ -455,38 +441,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           // this warp's CW columns = queries qlo .. of group g (whole queries: CW % H == 0);
           // per-warp base pointers so that every shared load below has a constant offset
           const int qlo = g * G + (sub * CW) / H;
-          const float* wrow = wq_s + qlo * H;  // weight of column c is wrow[c]
+          // halved weight of column c is wrow[c]: read through L1 with a warp-uniform
+          // address (one request per load; a shared-memory broadcast of 128-bit
+          // values costs four wavefronts)
+          const float* wrow =
+              a.wq + ((size_t)(MODE == 0 ? 0 : a.row0) + (size_t)itm.block * QB + qlo) * H;
           const int32_t* prow = pos_s + qlo;
           const float* trow = thr_s + qlo;
           const int32_t* rrow = row_s + qlo;
           HeadSum<H> hs;
           hs.reset();
-          float v[32];
-          tc::tmem_ld32(tbase, v);
-          tc::tmem_wait_ld(v);
-#pragma unroll
-          for (int ch = 0; ch < CW / 32; ++ch) {
-            if (ch > 0) {
-              tc::tmem_ld32(tbase + ch * 32, v);
-              tc::tmem_wait_ld(v);
-            }
+          constexpr int NCH = CW / kChunk;
+          float va[kChunk], vb[kLookahead ? kChunk : 1];
+          tc::tmem_ld_n(tbase, va);
+          tc::tmem_wait_ld(va);
+          auto reduce = [&](const float (&v)[kChunk], int ch) {
             constexpr int STEP = H == 1 ? 1 : (H == 2 ? 2 : 4);
 #pragma unroll
-            for (int j = 0; j < 32; j += STEP) {
-              const int col = ch * 32 + j;  // column within this warp's span
-              const int qi = col / H;       // query within the span
+            for (int j = 0; j < kChunk; j += STEP) {
+              const int col = ch * kChunk + j;  // column within this warp's span
+              const int qi = col / H;           // query within the span
               const int h = col % H;
               float sc = 0.0f;
               bool done = false;
               if (H == 1) {
-                sc = single_head_score<H>(v[j], wrow[col]);
+                sc = single_head_score<H>(v[j], __ldg(wrow + col));
                 done = true;
               } else if (H == 2) {
-                const float2 w2 = *reinterpret_cast<const float2*>(wrow + col);
+                const float2 w2 = __ldg(reinterpret_cast<const float2*>(wrow + col));
                 hs.add_pair(h, v[j], v[j + 1], w2.x, w2.y);
                 done = true;
               } else {
-                const float4 w4 = *reinterpret_cast<const float4*>(wrow + col);
+                const float4 w4 = __ldg(reinterpret_cast<const float4*>(wrow + col));
                 hs.add_pair(h, v[j], v[j + 1], w4.x, w4.y);
                 hs.add_pair(h + 2, v[j + 2], v[j + 3], w4.z, w4.w);
                 done = (h + 4 == H);
@@ -508,6 +494,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a.table[(size_t)r * a.L + s] = (s <= p) ? sc : -__int_as_float(0x7f800000);
                 }
               }
+            }
+          };
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
+            if constexpr (kLookahead) {
+              float (&cur)[kChunk] = (ch & 1) ? *reinterpret_cast<float(*)[kChunk]>(vb) : va;
+              float (&nxt)[kChunk] = (ch & 1) ? va : *reinterpret_cast<float(*)[kChunk]>(vb);
+              if (ch + 1 < NCH) tc::tmem_ld_n(tbase + (ch + 1) * kChunk, nxt);
+              reduce(cur, ch);
+              if (ch + 1 < NCH) tc::tmem_wait_ld(nxt);
+            } else {
+              if (ch > 0) {
+                tc::tmem_ld_n(tbase + ch * kChunk, va);
+                tc::tmem_wait_ld(va);
+              }
+              reduce(va, ch);
             }
           }
           tc::fence_before_sync();

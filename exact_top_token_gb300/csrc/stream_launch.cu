@@ -69,8 +69,8 @@ cudaError_t launch_filter(const Problem& p, const SelectWs& ws, int reverse, cud
   return dispatch(p, 0, km, qm, a, num_sms(), st);
 }
 
-cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, uint32_t* status,
-                         cudaStream_t st) {
+cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, const float* hw,
+                         uint32_t* status, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int es = p.dt == 0 ? 2 : 1;
   CUtensorMap km, qm;
@@ -79,6 +79,7 @@ cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, uin
                     atom_bytes(p)))
     return cudaErrorInvalidValue;
   stream::Args a{};
+  a.wq = hw;
   a.w = p.w;
   a.q_scale = p.q_scale;
   a.positions = p.positions;

@@ -185,6 +185,14 @@ __device__ __forceinline__ void tmem_wait_ld(float (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]), "+f"(v[15]) : : "memory");
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, float (&v)[N]) {
+  static_assert(N == 16 || N == 32 || N == 64, "chunk");
+  if constexpr (N == 64) tmem_ld64(taddr, v);
+  else if constexpr (N == 32) tmem_ld32(taddr, v);
+  else tmem_ld16(taddr, v);
+}
+
 // ---- MMA ---------------------------------------------------------------------------
 
 // D[tmem] (+)= A[smem] * B[smem]^T, A: M x K (K-major), B: N x K (K-major).
