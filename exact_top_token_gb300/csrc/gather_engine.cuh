@@ -178,6 +178,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       }
     }
     const int ntiles = (nrows + kTileKeys - 1) / kTileKeys;
+    // key of row j of this query's list (replay: the stored index, unchecked)
+    auto key_of = [&](int j) -> int {
+      if (j >= nrows) return -1;
+      if (MODE == kThreshold) return step.at(j);
+      if (MODE == kReplay) return __ldg(a.idx + (size_t)t * a.k_top + j);
+      return j;
+    };
 
     // ---- the query operand (H rows of d, zero-padded to NQ) and weights ----
     {
@@ -209,21 +216,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       // ---------------- producers: gather 128 key rows per tile ----------------
       const int tid = threadIdx.x;
       int npend = 0;
+      // one row per producer thread; its keys are fetched two tiles ahead
+      int s_next = key_of(tid), s_next2 = key_of(kTileKeys + tid);
       for (int i = 0; i < ntiles; ++i) {
+        int s = s_next;
+        s_next = s_next2;
+        s_next2 = key_of((i + 2) * kTileKeys + tid);
         if (!tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status)) break;
         uint8_t* dst = ring + p_stage * C_::KT_BYTES;
         {
-          // one row per producer thread: its key position, then its d bytes
           const int row = tid;
-          const int j = i * kTileKeys + row;
-          int s = -1;
-          if (j < nrows) {
-            if (MODE == kThreshold) s = step.at(j);
-            else if (MODE == kReplay) {
-              s = __ldg(a.idx + (size_t)t * a.k_top + j);
-              if (s < 0 || s >= a.L) s = -1;
-            } else s = j;
-          }
+          if (s >= a.L) s = -1;  // stored indices outside [0, L) gather nothing
           const uint8_t* src =
               reinterpret_cast<const uint8_t*>(a.k) + (s >= 0 ? (size_t)s * RB : 0);
 #pragma unroll
@@ -285,20 +288,24 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       // ---------------- epilogue: one key per thread ----------------
       const int quad = warp & 3;
       const int row = quad * 32 + lane;
+      // keys two tiles ahead and key scales one tile ahead of their use
+      auto scale_of = [&](int s) -> float {
+        return DT == 1 ? ((s >= 0 && s < a.L) ? __ldg(a.k_scale + s) : 0.0f) : 1.0f;
+      };
+      int s_next = key_of(row), s_next2 = key_of(kTileKeys + row);
+      float ks_next = scale_of(s_next);
       for (int i = 0; i < ntiles; ++i) {
+        const int s = s_next;
+        const float ks = ks_next;
+        s_next = s_next2;
+        ks_next = scale_of(s_next);
+        s_next2 = key_of((i + 2) * kTileKeys + row);
         if (!tc::mbar_wait(acc_full + e_slot, e_aphase, abort_flag, a.status)) break;
         tc::fence_after_sync();
         const uint32_t taddr =
             tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(e_slot * NQ);
         const int j = i * kTileKeys + row;
-        int s = -1;
-        if (j < nrows) {
-          if (MODE == kThreshold) s = step.at(j);
-          else if (MODE == kReplay) s = __ldg(a.idx + (size_t)t * a.k_top + j);
-          else s = j;
-        }
         const bool valid = s >= 0 && s < a.L;
-        const float ks = DT == 1 ? (valid ? __ldg(a.k_scale + s) : 0.0f) : 1.0f;
         stream::HeadSum<H> hs;
         hs.reset();
         float sc;
