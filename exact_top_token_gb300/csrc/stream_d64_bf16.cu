@@ -13,7 +13,9 @@ cudaError_t go(const CUtensorMap& km, const CUtensorMap& qm, const stream::Args&
                cudaStream_t st) {
   constexpr int smem = stream::Cfg<64, 0, H>::SMEM;
   auto fn = stream::k_stream<64, 0, H, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = stream::check_register_split<64, 0, H, MODE>();
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   fn<<<grid, stream::kThreads, smem, st>>>(km, qm, a);
   return cudaGetLastError();

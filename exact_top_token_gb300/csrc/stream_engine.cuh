@@ -11,15 +11,18 @@
 // One persistent CTA per SM walks items blockIdx.x, +gridDim.x, ... in
 // chunk-major order, so the CTAs running at one time share a key chunk in L2.
 //
-//   warp 0  TMA producer: the block's q rows (NG groups of 256 (query, head)
-//           rows) once per item, then the key tiles through a STAGES ring.
-//   warp 1  MMA issuer: per key tile and group, one 128 x 256 x d product
-//           (keys x (query, head)) into one of two TMEM accumulators.
-//   warp 2  TMEM allocator.
+//   warp 0  TMA producer: the block's q rows (256 (query, head) rows) once
+//           per item, then the key tiles through a STAGES ring.
+//   warp 1  TMEM allocator and MMA issuer: per key tile one 128 x 256 x d
+//           product (keys x (query, head)) into one of two TMEM accumulators.
+//   warps 2, 3 idle (they complete warpgroup 0, which hands registers to the
+//           epilogue warpgroups with setmaxnreg).
 //   warps 4..19 epilogue: TMEM lane = key, so each thread reduces its key's
 //           H heads per query in registers: ReLU, times w*q_scale (packed
 //           fp32 FMA), times k_scale; then the causal test and the threshold
 //           test, and a warp-aggregated append to the candidate buffer.
+//           A warp always reads the same 64 accumulator columns during an
+//           item, so (for H <= 64) it keeps their weights in registers.
 #pragma once
 
 #include "tc.cuh"
@@ -30,9 +33,18 @@ namespace stream {
 constexpr int kChunkTiles = 64;
 constexpr int kChunkKeys = kChunkTiles * kTileKeys;
 constexpr int kEpiWarps = 16;   // epilogue warps (4 per TMEM lane quadrant)
-constexpr int kChunk = 32;      // TMEM columns per tcgen05.ld in the epilogue
-constexpr bool kLookahead = false;  // load chunk c+1 while reducing chunk c
-constexpr int kThreads = 128 + kEpiWarps * 32;
+constexpr int kEpiWarp0 = 4;    // first epilogue warp: warpgroups 1..4 are the epilogue
+constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
+// Register split. One CTA of kThreads per SM is launched with kRegsLaunch
+// registers a thread (65536 / 640, rounded down to a multiple of 8); then
+// warpgroup 0 shrinks to kRegsCtl and the epilogue warpgroups grow to kRegsEpi.
+// setmaxnreg.inc waits until the CTA's pool (threads x launch registers) can
+// serve it, so the split must fit in that pool.
+constexpr int kRegsLaunch = 96;
+constexpr int kRegsCtl = 32;
+constexpr int kRegsEpi = 112;
+static_assert(128 * kRegsCtl + (kThreads - 128) * kRegsEpi <= kThreads * kRegsLaunch,
+              "register split exceeds the CTA's launch allocation");
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (and its 512 TMEM columns) per SM
 
 template <int D, int DT, int H, int MODE_STAGING = 1>
@@ -41,11 +53,11 @@ struct Cfg {
   static constexpr int RB = D * ES;
   using Geo = tc::Geo<RB>;
   static constexpr int G = 256 / H;               // queries per MMA (N = 256 columns)
-  static constexpr int NG = RB == 256 ? 1 : 2;    // MMA groups per work item
+  static constexpr int NG = 1;                    // MMA groups per work item
   static constexpr int QB = G * NG;               // query slots per work item
   static constexpr int KT_BYTES = 128 * RB;
   static constexpr int QG_BYTES = 256 * RB;
-  static constexpr int STAGES = RB == 256 ? 3 : (RB == 128 ? 4 : 8);
+  static constexpr int STAGES = RB == 256 ? 4 : (RB == 128 ? 6 : 8);
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NG * QG_BYTES;
   static constexpr int BAR_OFF = K_OFF + STAGES * KT_BYTES;
@@ -63,6 +75,9 @@ struct Cfg {
   // epilogue: each warp owns one TMEM lane quadrant (32 keys) and CW columns
   static constexpr int CW = H > (1024 / kEpiWarps) ? H : (1024 / kEpiWarps);
   static constexpr int ACTIVE_EPI = 4 * (256 / CW);  // warps that read accumulators
+  // weights of the CW columns kept in registers for a whole item (H <= 64)
+  static constexpr bool REG_W = CW == 64;
+  static constexpr int KC = REG_W ? 16 : 32;  // TMEM columns per tcgen05.ld
   static_assert(H >= 1 && H <= 128 && (H & (H - 1)) == 0, "H must be a power of two <= 128");
   static_assert(RB == 64 || RB == 128 || RB == 256, "row bytes");
 };
@@ -151,6 +166,14 @@ struct HeadSum {
     asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(hw0), "f"(hw1));
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a[s]) : "l"(r), "l"(w));
   }
+  // the same with the two halved weights already packed as {hw0, hw1}
+  __device__ __forceinline__ void add_pair_packed(int h, float x0, float x1, uint64_t w) {
+    const int s = (h >> 1) % NA;
+    const float r0 = x0 + fabsf(x0), r1 = x1 + fabsf(x1);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(r0), "f"(r1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a[s]) : "l"(r), "l"(w));
+  }
   __device__ __forceinline__ float lane_sum(int i) const {
     float lo, hi;
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a[i]));
@@ -222,6 +245,21 @@ __device__ __forceinline__ void flush_staged(int block, uint32_t* scnt, const ui
 template <int D, int DT, int H, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_stream(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+             const Args a);
+
+// Host side: a build whose launch register count is below kRegsLaunch would
+// leave the epilogue's setmaxnreg.inc unserved, so it is refused before launch.
+template <int D, int DT, int H, int MODE>
+inline cudaError_t check_register_split() {
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, k_stream<D, DT, H, MODE>);
+  if (e != cudaSuccess) return e;
+  return fa.numRegs >= kRegsLaunch ? cudaSuccess : cudaErrorLaunchOutOfResources;
+}
+
+template <int D, int DT, int H, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_stream(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
              const Args a) {
   using C_ = Cfg<D, DT, H, MODE == 0 ? 1 : 0>;
   using Geo = typename C_::Geo;
@@ -264,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     tc::tmem_alloc(tmem_slot, 512);
     tc::tmem_relinquish();
   }
@@ -275,120 +313,131 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto item_at = [&](int i) { return a.reverse ? total - 1 - i : i; };
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      tc::tma_prefetch(&kmap);
-      tc::tma_prefetch(&qmap);
-      int stage = 0;
-      uint32_t sphase = 0, qphase = 0;
-      uint32_t pending = 0, pend_phase = 0, q_loads = 0;  // issued loads, for a clean abort
-      for (int i = blockIdx.x; i < total; i += gridDim.x) {
-        const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
-        if (!tc::mbar_wait(q_empty, qphase ^ 1u, abort_flag, a.status)) break;
-        qphase ^= 1u;
-        tc::mbar_expect_tx(q_full, NG * C_::QG_BYTES);
-        const int qrow0 = (MODE == 0 ? itm.block * QB : a.row0 + itm.block * QB) * H;
-#pragma unroll
-        for (int g = 0; g < NG; ++g)
-#pragma unroll
-          for (int at = 0; at < Geo::kAtoms; ++at)
-            tc::tma_load_2d(smem + C_::Q_OFF + g * C_::QG_BYTES + at * 256 * Geo::kAtom, &qmap,
-                            q_full, at * Geo::kAtom / C_::ES, qrow0 + g * 256);
-        ++q_loads;
-        bool ok = true;
-        for (int t = 0; t < itm.ntiles; ++t) {
-          if (!tc::mbar_wait(k_empty + stage, sphase ^ 1u, abort_flag, a.status)) {
-            ok = false;
-            break;
+  // Each role starts with its setmaxnreg, so that the register target of its
+  // code is the one set there.
+  if (warp < kEpiWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if (warp == 0) {
+      if (lane == 0) {
+        // ---------------- TMA producer ----------------
+        tc::tma_prefetch(&kmap);
+        tc::tma_prefetch(&qmap);
+        int stage = 0;
+        uint32_t sphase = 0, qphase = 0;
+        uint32_t pending = 0, pend_phase = 0, q_loads = 0;  // issued loads, for a clean abort
+        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+          const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
+          if (!tc::mbar_wait(q_empty, qphase ^ 1u, abort_flag, a.status)) break;
+          qphase ^= 1u;
+          tc::mbar_expect_tx(q_full, NG * C_::QG_BYTES);
+          const int qrow0 = (MODE == 0 ? itm.block * QB : a.row0 + itm.block * QB) * H;
+  #pragma unroll
+          for (int g = 0; g < NG; ++g)
+  #pragma unroll
+            for (int at = 0; at < Geo::kAtoms; ++at)
+              tc::tma_load_2d(smem + C_::Q_OFF + g * C_::QG_BYTES + at * 256 * Geo::kAtom, &qmap,
+                              q_full, at * Geo::kAtom / C_::ES, qrow0 + g * 256);
+          ++q_loads;
+          bool ok = true;
+          for (int t = 0; t < itm.ntiles; ++t) {
+            if (!tc::mbar_wait(k_empty + stage, sphase ^ 1u, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc::mbar_expect_tx(k_full + stage, C_::KT_BYTES);
+  #pragma unroll
+            for (int at = 0; at < Geo::kAtoms; ++at)
+              tc::tma_load_2d(smem + C_::K_OFF + stage * C_::KT_BYTES + at * 128 * Geo::kAtom,
+                              &kmap, k_full + stage, at * Geo::kAtom / C_::ES,
+                              (itm.tile0 + t) * kTileKeys);
+            pending |= 1u << stage;
+            pend_phase = (pend_phase & ~(1u << stage)) | (sphase << stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              sphase ^= 1u;
+            }
           }
-          tc::mbar_expect_tx(k_full + stage, C_::KT_BYTES);
-#pragma unroll
-          for (int at = 0; at < Geo::kAtoms; ++at)
-            tc::tma_load_2d(smem + C_::K_OFF + stage * C_::KT_BYTES + at * 128 * Geo::kAtom,
-                            &kmap, k_full + stage, at * Geo::kAtom / C_::ES,
-                            (itm.tile0 + t) * kTileKeys);
-          pending |= 1u << stage;
-          pend_phase = (pend_phase & ~(1u << stage)) | (sphase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            sphase ^= 1u;
-          }
+          if (!ok) break;
         }
-        if (!ok) break;
-      }
-      if (*abort_flag) {
-        // let the copies still in flight land before the CTA exits (bounded)
-        const uint64_t t0 = tc::global_ns();
-        for (int st = 0; st < STAGES; ++st)
-          if (pending & (1u << st))
-            while (!tc::mbar_try_wait(k_full + st, (pend_phase >> st) & 1u) &&
+        if (*abort_flag) {
+          // let the copies still in flight land before the CTA exits (bounded)
+          const uint64_t t0 = tc::global_ns();
+          for (int st = 0; st < STAGES; ++st)
+            if (pending & (1u << st))
+              while (!tc::mbar_try_wait(k_full + st, (pend_phase >> st) & 1u) &&
+                     tc::global_ns() - t0 < 200000000ull) {
+              }
+          if (q_loads)
+            while (!tc::mbar_try_wait(q_full, (q_loads - 1) & 1u) &&
                    tc::global_ns() - t0 < 200000000ull) {
             }
-        if (q_loads)
-          while (!tc::mbar_try_wait(q_full, (q_loads - 1) & 1u) &&
-                 tc::global_ns() - t0 < 200000000ull) {
-          }
+        }
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      constexpr uint32_t IDESC = tc::instr_desc(DT, 128, 256);
-      const uint32_t q_addr = tc::smem_u32(smem + C_::Q_OFF);
-      const uint32_t k_addr = tc::smem_u32(smem + C_::K_OFF);
-      int stage = 0, acc = 0;
-      uint32_t sphase = 0, aphase = 0, qphase = 0;
-      for (int i = blockIdx.x; i < total; i += gridDim.x) {
-        const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
-        if (!tc::mbar_wait(q_full, qphase, abort_flag, a.status)) break;
-        qphase ^= 1u;
-        tc::fence_after_sync();
-        bool ok = true;
-        for (int t = 0; t < itm.ntiles && ok; ++t) {
-          if (!tc::mbar_wait(k_full + stage, sphase, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
+    } else if (warp == 1) {
+      if (lane == 0) {
+        // ---------------- MMA issuer ----------------
+        constexpr uint32_t IDESC = tc::instr_desc(DT, 128, 256);
+        const uint32_t q_addr = tc::smem_u32(smem + C_::Q_OFF);
+        const uint32_t k_addr = tc::smem_u32(smem + C_::K_OFF);
+        int stage = 0, acc = 0;
+        uint32_t sphase = 0, aphase = 0, qphase = 0;
+        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+          const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
+          if (!tc::mbar_wait(q_full, qphase, abort_flag, a.status)) break;
+          qphase ^= 1u;
           tc::fence_after_sync();
-#pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            if (!tc::mbar_wait(acc_empty + acc, aphase ^ 1u, abort_flag, a.status)) {
+          bool ok = true;
+          for (int t = 0; t < itm.ntiles && ok; ++t) {
+            if (!tc::mbar_wait(k_full + stage, sphase, abort_flag, a.status)) {
               ok = false;
               break;
             }
             tc::fence_after_sync();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
-#pragma unroll
-            for (int j = 0; j < Geo::kSteps; ++j) {
-              const uint64_t adesc = tc::smem_desc(
-                  k_addr + stage * C_::KT_BYTES + Geo::step_offset(j, 128), Geo::kSbo, Geo::kSwizzle);
-              const uint64_t bdesc = tc::smem_desc(
-                  q_addr + g * C_::QG_BYTES + Geo::step_offset(j, 256), Geo::kSbo, Geo::kSwizzle);
-              tc::mma<DT>(d_tmem, adesc, bdesc, IDESC, j > 0 ? 1u : 0u);
+  #pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              if (!tc::mbar_wait(acc_empty + acc, aphase ^ 1u, abort_flag, a.status)) {
+                ok = false;
+                break;
+              }
+              tc::fence_after_sync();
+              const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+  #pragma unroll
+              for (int j = 0; j < Geo::kSteps; ++j) {
+                const uint64_t adesc = tc::smem_desc(
+                    k_addr + stage * C_::KT_BYTES + Geo::step_offset(j, 128), Geo::kSbo, Geo::kSwizzle);
+                const uint64_t bdesc = tc::smem_desc(
+                    q_addr + g * C_::QG_BYTES + Geo::step_offset(j, 256), Geo::kSbo, Geo::kSwizzle);
+                tc::mma<DT>(d_tmem, adesc, bdesc, IDESC, j > 0 ? 1u : 0u);
+              }
+              tc::mma_commit(acc_full + acc);
+              acc ^= 1;
+              if (acc == 0) aphase ^= 1u;
             }
-            tc::mma_commit(acc_full + acc);
-            acc ^= 1;
-            if (acc == 0) aphase ^= 1u;
+            tc::mma_commit(k_empty + stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              sphase ^= 1u;
+            }
           }
-          tc::mma_commit(k_empty + stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            sphase ^= 1u;
-          }
+          tc::mma_commit(q_empty);
+          if (!ok) break;
         }
-        tc::mma_commit(q_empty);
-        if (!ok) break;
       }
     }
-  } else if (warp >= 4) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
     // ---------------- epilogue ----------------
     constexpr int CW = C_::CW;
-    const int e = warp - 4;
-    const int quad = warp & 3;
-    const int sub = e >> 2;                 // column span of this warp: [sub*CW, sub*CW+CW)
+    constexpr int KC = C_::KC;
+    constexpr bool REG_W = C_::REG_W;
+    constexpr int NQS = CW / H;           // queries in a warp's column span
+    constexpr bool REG_META = NQS <= 4;   // their position and threshold in registers
+    const int e = warp - kEpiWarp0;
+    const int quad = warp & 3;            // TMEM lane quadrant this warp may read
+    const int sub = e >> 2;               // column span of this warp: [sub*CW, sub*CW+CW)
     const bool reads_tmem = sub * CW < 256;
-    const int et = threadIdx.x - 128;
+    const int qlo = (sub * CW) / H;       // first query (within the block) of the span
+    const int et = threadIdx.x - kEpiWarp0 * 32;
     int acc = 0;
     uint32_t aphase = 0;
     int prev_block = -1;
@@ -419,6 +468,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       epi_sync();
       if (*abort_flag || !reads_tmem) continue;  // named-barrier count stays equal
+      // halved weight of column c of the span is wrow[c] (workspace, warp-uniform)
+      const float* wrow =
+          a.wq + ((size_t)(MODE == 0 ? 0 : a.row0) + (size_t)itm.block * QB + qlo) * H;
+      const int32_t* prow = pos_s + qlo;
+      const float* trow = thr_s + qlo;
+      const int32_t* rrow = row_s + qlo;
+      // per item: the span's weights as packed pairs {hw[2c], hw[2c+1]}, and the
+      // positions and thresholds of its queries
+      uint64_t wp[REG_W ? CW / 2 : 1];
+      if constexpr (REG_W) {
+        if (MODE == 0) {  // slot rows: 256-byte aligned
+#pragma unroll
+          for (int u = 0; u < CW / 4; ++u) {
+            const ulonglong2 w2 = __ldg(reinterpret_cast<const ulonglong2*>(wrow) + u);
+            wp[2 * u] = w2.x;
+            wp[2 * u + 1] = w2.y;
+          }
+        } else {  // rows from an arbitrary row0: 4-byte aligned only
+#pragma unroll
+          for (int u = 0; u < CW / 2; ++u)
+            asm("mov.b64 %0, {%1, %2};"
+                : "=l"(wp[u])
+                : "f"(__ldg(wrow + 2 * u)), "f"(__ldg(wrow + 2 * u + 1)));
+        }
+      }
+      int pv[REG_META ? NQS : 1];
+      float tv[REG_META ? NQS : 1];
+      if constexpr (REG_META) {
+#pragma unroll
+        for (int u = 0; u < NQS; ++u) {
+          pv[u] = prow[u];
+          tv[u] = trow[u];
+        }
+      }
       bool ok = true;
       const int s_first = itm.tile0 * kTileKeys + quad * 32 + lane;
       float ks_next = DT == 1 ? (s_first < a.L ? __ldg(a.k_scale + s_first) : 0.0f) : 1.0f;
@@ -429,95 +512,84 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sn = s + kTileKeys;
           ks_next = (t + 1 < itm.ntiles && sn < a.L) ? __ldg(a.k_scale + sn) : 0.0f;
         }
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          if (!tc::mbar_wait(acc_full + acc, aphase, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t tbase =
-              tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + sub * CW);
-          // this warp's CW columns = queries qlo .. of group g (whole queries: CW % H == 0);
-          // per-warp base pointers so that every shared load below has a constant offset
-          const int qlo = g * G + (sub * CW) / H;
-          // halved weight of column c is wrow[c]: read through L1 with a warp-uniform
-          // address (one request per load; a shared-memory broadcast of 128-bit
-          // values costs four wavefronts)
-          const float* wrow =
-              a.wq + ((size_t)(MODE == 0 ? 0 : a.row0) + (size_t)itm.block * QB + qlo) * H;
-          const int32_t* prow = pos_s + qlo;
-          const float* trow = thr_s + qlo;
-          const int32_t* rrow = row_s + qlo;
-          HeadSum<H> hs;
-          hs.reset();
-          constexpr int NCH = CW / kChunk;
-          float va[kChunk], vb[kLookahead ? kChunk : 1];
-          tc::tmem_ld_n(tbase, va);
-          tc::tmem_wait_ld(va);
-          auto reduce = [&](const float (&v)[kChunk], int ch) {
-            constexpr int STEP = H == 1 ? 1 : (H == 2 ? 2 : 4);
-#pragma unroll
-            for (int j = 0; j < kChunk; j += STEP) {
-              const int col = ch * kChunk + j;  // column within this warp's span
-              const int qi = col / H;           // query within the span
-              const int h = col % H;
-              float sc = 0.0f;
-              bool done = false;
-              if (H == 1) {
-                sc = single_head_score<H>(v[j], __ldg(wrow + col));
-                done = true;
-              } else if (H == 2) {
-                const float2 w2 = __ldg(reinterpret_cast<const float2*>(wrow + col));
-                hs.add_pair(h, v[j], v[j + 1], w2.x, w2.y);
-                done = true;
-              } else {
-                const float4 w4 = __ldg(reinterpret_cast<const float4*>(wrow + col));
-                hs.add_pair(h, v[j], v[j + 1], w4.x, w4.y);
-                hs.add_pair(h + 2, v[j + 2], v[j + 3], w4.z, w4.w);
-                done = (h + 4 == H);
-              }
-              if (done) {
-                if (H >= 2) {
-                  sc = hs.total();
-                  hs.reset();
-                }
-                sc = finish_score(sc, ks);
-                const int p = prow[qi];
-                if (MODE == 0) {
-                  const bool pass = (s <= p) && (sc >= trow[qi]);
-                  append_staged<CAP>(pass, sc, s, qlo + qi, rrow[qi], scnt_s, stage_s, a.cnt,
-                                     a.cand, a.C);
-                } else {
-                  const int r = rrow[qi];
-                  if (r >= 0 && s < a.L)
-                    a.table[(size_t)r * a.L + s] = (s <= p) ? sc : -__int_as_float(0x7f800000);
-                }
-              }
-            }
-          };
-#pragma unroll
-          for (int ch = 0; ch < NCH; ++ch) {
-            if constexpr (kLookahead) {
-              float (&cur)[kChunk] = (ch & 1) ? *reinterpret_cast<float(*)[kChunk]>(vb) : va;
-              float (&nxt)[kChunk] = (ch & 1) ? va : *reinterpret_cast<float(*)[kChunk]>(vb);
-              if (ch + 1 < NCH) tc::tmem_ld_n(tbase + (ch + 1) * kChunk, nxt);
-              reduce(cur, ch);
-              if (ch + 1 < NCH) tc::tmem_wait_ld(nxt);
-            } else {
-              if (ch > 0) {
-                tc::tmem_ld_n(tbase + ch * kChunk, va);
-                tc::tmem_wait_ld(va);
-              }
-              reduce(va, ch);
-            }
-          }
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(acc_empty + acc);
-          acc ^= 1;
-          if (acc == 0) aphase ^= 1u;
+        if (!tc::mbar_wait(acc_full + acc, aphase, abort_flag, a.status)) {
+          ok = false;
+          break;
         }
+        tc::fence_after_sync();
+        const uint32_t tbase =
+            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + sub * CW);
+        HeadSum<H> hs;
+        hs.reset();
+        float va[KC];
+        auto reduce = [&](const float (&v)[KC], int ch) {
+          constexpr int STEP = H == 1 ? 1 : (H == 2 ? 2 : 4);
+#pragma unroll
+          for (int j = 0; j < KC; j += STEP) {
+            const int col = ch * KC + j;  // column within this warp's span
+            const int qi = col / H;       // query within the span
+            const int h = col % H;
+            float sc = 0.0f;
+            bool done = false;
+            if (H == 1) {
+              float hw;
+              if constexpr (REG_W) {
+                float lo, hi;
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(wp[col / 2]));
+                hw = (col & 1) ? hi : lo;
+              } else {
+                hw = __ldg(wrow + col);
+              }
+              sc = single_head_score<H>(v[j], hw);
+              done = true;
+            } else if (REG_W) {
+              hs.add_pair_packed(h, v[j], v[j + 1], wp[col / 2]);
+              if (H >= 4) hs.add_pair_packed(h + 2, v[j + 2], v[j + 3], wp[col / 2 + 1]);
+              done = (h + STEP == H);
+            } else {
+              const float4 w4 = __ldg(reinterpret_cast<const float4*>(wrow + col));
+              hs.add_pair(h, v[j], v[j + 1], w4.x, w4.y);
+              hs.add_pair(h + 2, v[j + 2], v[j + 3], w4.z, w4.w);
+              done = (h + 4 == H);
+            }
+            if (done) {
+              if (H >= 2) {
+                sc = hs.total();
+                hs.reset();
+              }
+              sc = finish_score(sc, ks);
+              int p;
+              float thr;
+              if constexpr (REG_META) {
+                p = pv[qi];
+                thr = tv[qi];
+              } else {
+                p = prow[qi];
+                thr = trow[qi];
+              }
+              if (MODE == 0) {
+                const bool pass = (s <= p) && (sc >= thr);
+                append_staged<CAP>(pass, sc, s, qlo + qi, rrow[qi], scnt_s, stage_s, a.cnt,
+                                   a.cand, a.C);
+              } else {
+                const int r = rrow[qi];
+                if (r >= 0 && s < a.L)
+                  a.table[(size_t)r * a.L + s] = (s <= p) ? sc : -__int_as_float(0x7f800000);
+              }
+            }
+          }
+        };
+#pragma unroll
+        for (int ch = 0; ch < CW / KC; ++ch) {
+          tc::tmem_ld_n(tbase + ch * KC, va);
+          tc::tmem_wait_ld(va);
+          reduce(va, ch);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(acc_empty + acc);
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1u;
       }
     }
     if (MODE == 0) {
@@ -528,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, 512);
   }

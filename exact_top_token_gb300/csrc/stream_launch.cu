@@ -37,10 +37,8 @@ bool key_map(const Problem& p, CUtensorMap* km) {
 
 }  // namespace
 
-int stream_query_block(int H, int d, int dt) {
-  const int rb = d * (dt == 0 ? 2 : 1);
-  return (256 / H) * (rb == 256 ? 1 : 2);
-}
+// one MMA group of 256 (query, head) columns per work item
+int stream_query_block(int H, int /*d*/, int /*dt*/) { return 256 / H; }
 
 cudaError_t launch_filter(const Problem& p, const SelectWs& ws, int reverse, cudaStream_t st) {
   if (ws.n_pad == 0) return cudaSuccess;
