@@ -35,11 +35,12 @@ constexpr int kChunkKeys = kChunkTiles * kTileKeys;
 constexpr int kEpiWarps = 16;   // epilogue warps (4 per TMEM lane quadrant)
 constexpr int kEpiWarp0 = 4;    // first epilogue warp: warpgroups 1..4 are the epilogue
 constexpr int kThreads = kEpiWarp0 * 32 + kEpiWarps * 32;
-// Register split. One CTA of kThreads per SM is launched with kRegsLaunch
-// registers a thread (65536 / 640, rounded down to a multiple of 8); then
-// warpgroup 0 shrinks to kRegsCtl and the epilogue warpgroups grow to kRegsEpi.
-// setmaxnreg.inc waits until the CTA's pool (threads x launch registers) can
-// serve it, so the split must fit in that pool.
+// One CTA of kThreads per SM is launched with kRegsLaunch registers a thread
+// (65536 / 640, rounded down to a multiple of 8). When the epilogue keeps its
+// weights in registers, warpgroup 0 then shrinks to kRegsCtl and the epilogue
+// warpgroups grow to kRegsEpi (setmaxnreg). setmaxnreg.inc waits until the
+// CTA's pool (threads x launch registers) can serve it, so the split must fit
+// in that pool.
 constexpr int kRegsLaunch = 96;
 constexpr int kRegsCtl = 32;
 constexpr int kRegsEpi = 112;
@@ -148,7 +149,10 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // (x + |x|) * hw: 2x and w/2 are exact scalings, so the product is bit for
 // bit ReLU(x) * w (for |w| >= 2^-125), while the add runs on the FMA pipe.
 // Head pair p = (2p, 2p+1) accumulates into packed accumulator p % NA with
-// one packed fp32 FMA; then total = ((s0 + s1) + (s2 + s3)), s_i = lo_i + hi_i.
+// one packed fp32 FMA (the first pair of each accumulator with a packed
+// multiply, which gives the same value up to the sign of a zero); then the
+// accumulators are combined with packed adds, t = (a0 + a1) + (a2 + a3), and
+// total = lo(t) + hi(t). The sign of a zero total is made +0 by finish_score.
 template <int H>
 struct HeadSum {
   static constexpr int NA = H >= 8 ? 4 : (H >= 2 ? H / 2 : 1);
@@ -166,13 +170,17 @@ struct HeadSum {
     asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(hw0), "f"(hw1));
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a[s]) : "l"(r), "l"(w));
   }
-  // the same with the two halved weights already packed as {hw0, hw1}
+  // the same with the two halved weights already packed as {hw0, hw1}; the
+  // first pair of an accumulator (h < 2 NA) sets it, so no reset is needed
   __device__ __forceinline__ void add_pair_packed(int h, float x0, float x1, uint64_t w) {
     const int s = (h >> 1) % NA;
     const float r0 = x0 + fabsf(x0), r1 = x1 + fabsf(x1);
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(r0), "f"(r1));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a[s]) : "l"(r), "l"(w));
+    if (h < 2 * NA)
+      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(a[s]) : "l"(r), "l"(w));
+    else
+      asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a[s]) : "l"(r), "l"(w));
   }
   __device__ __forceinline__ float lane_sum(int i) const {
     float lo, hi;
@@ -180,9 +188,17 @@ struct HeadSum {
     return lo + hi;
   }
   __device__ __forceinline__ float total() const {
-    if (NA == 4) return (lane_sum(0) + lane_sum(1)) + (lane_sum(2) + lane_sum(3));
-    if (NA == 2) return lane_sum(0) + lane_sum(1);
-    return lane_sum(0);
+    if (NA == 1) return lane_sum(0);
+    uint64_t t;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(a[0]), "l"(a[1]));
+    if (NA == 4) {
+      uint64_t t23;
+      asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t23) : "l"(a[2]), "l"(a[3]));
+      asm("add.rn.f32x2 %0, %0, %1;" : "+l"(t) : "l"(t23));
+    }
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(t));
+    return lo + hi;
   }
 };
 
@@ -316,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Each role starts with its setmaxnreg, so that the register target of its
   // code is the one set there.
   if (warp < kEpiWarp0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
+    if constexpr (C_::REG_W) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsCtl));
     if (warp == 0) {
       if (lane == 0) {
         // ---------------- TMA producer ----------------
@@ -425,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+    if constexpr (C_::REG_W) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
     // ---------------- epilogue ----------------
     constexpr int CW = C_::CW;
     constexpr int KC = C_::KC;
@@ -520,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tbase =
             tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + sub * CW);
         HeadSum<H> hs;
-        hs.reset();
+        if (!REG_W) hs.reset();
         float va[KC];
         auto reduce = [&](const float (&v)[KC], int ch) {
           constexpr int STEP = H == 1 ? 1 : (H == 2 ? 2 : 4);
@@ -555,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (done) {
               if (H >= 2) {
                 sc = hs.total();
-                hs.reset();
+                if (!REG_W) hs.reset();
               }
               sc = finish_score(sc, ks);
               int p;
