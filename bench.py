@@ -95,8 +95,37 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def sum_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def pairs_of(case):
     return int((case["positions"].astype(np.int64) + 1).sum())
+
+
+def shard_case(case, world, rank):
+    """Rank `rank`'s shard of a global batch of world x n queries over the same
+    keys (weak scaling: every rank keeps n queries, no data-path collective).
+    For workloads whose queries sit at the last n positions, the global batch is
+    the last world x n positions and rank r takes the r-th block of n counted
+    from the end; other workloads give every rank the same positions."""
+    if world == 1:
+        return case
+    n = len(case["positions"])
+    L = int(case["k"].shape[0])
+    last = np.arange(L - n, L, dtype=np.int32)
+    if world * n <= L and np.array_equal(case["positions"], last):
+        out = dict(case)
+        out["positions"] = (last - rank * n).astype(np.int32)
+        return out
+    return case
 
 
 def peaks():
@@ -211,12 +240,16 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(case):
+def workload_config(case, world=1):
     n, H, d = case["q"].shape
-    return {"workload": case["name"], "L": int(case["k"].shape[0]), "n": int(n), "H": int(H),
-            "d": int(d), "k_top": int(case["k_top"]), "capacity": 8 * int(case["k_top"]),
-            "positions": "last n" if case["name"] == "glm_1m" else "see synthetic_inputs",
-            "l2": "inputs larger than L2 (K 128 MiB + Q 64 MiB + 1 GiB candidate buffer per step)"}
+    cfg = {"workload": case["name"], "L": int(case["k"].shape[0]), "n": int(n), "H": int(H),
+           "d": int(d), "k_top": int(case["k_top"]), "capacity": 8 * int(case["k_top"]),
+           "positions": "last n" if case["name"] == "glm_1m" else "see synthetic_inputs",
+           "l2": "inputs larger than L2 (K 128 MiB + Q 64 MiB + 1 GiB candidate buffer per step)"}
+    if world > 1:
+        cfg["parallelism"] = (f"dp{world}: query shards of n per GPU (rank r: the r-th block of n "
+                              "positions from the end), keys replicated, no collective")
+    return cfg
 
 
 # ---- the GPU arm -------------------------------------------------------------------------
@@ -240,10 +273,12 @@ def gpu_arm(args, world, rank, local):
     if args.queries:
         case = si.subset(case, np.arange(len(case["positions"]) - args.queries,
                                          len(case["positions"])))
+    case = shard_case(case, world, rank)
     n, H, d = case["q"].shape
     L = case["k"].shape[0]
     k_top = case["k_top"]
     pairs = pairs_of(case)
+    pairs_all = sum_over_ranks(pairs, world, dev)
     t = si.to_torch(case, dev)
     dt_code = hk.E4M3 if case["dtype"] == "e4m3" else hk.BF16
     ws = torch.empty(hk.select_workspace_size(n, L, H, d, k_top, 0, dt_code), dtype=torch.uint8,
@@ -319,10 +354,10 @@ def gpu_arm(args, world, rank, local):
               "achieved_gbs": replay_bytes / (replay_ms / 1e3) / 1e9,
               "frac_hbm_of_measured": replay_bytes / (replay_ms / 1e3) / 1e9 / pk["hbm_gbs"]}
 
-    line = {"metric": METRIC, "value": world * pairs / (ms_step / 1e3), "unit": "pairs/s",
+    line = {"metric": METRIC, "value": pairs_all / (ms_step / 1e3), "unit": "pairs/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": case["dtype"], "data": "synthetic", "config": workload_config(case),
+            "dtype": case["dtype"], "data": "synthetic", "config": workload_config(case, world),
             "clocks": clk, "gpu_launches": launches_per_step(case["dtype"]) * args.steps,
             "roofline": roofline, "select_ms": select_ms, "phases_ms": phase_ms,
             "replay": replay, "peaks": pk}
@@ -377,7 +412,8 @@ def e2e(args, hk, case, dev, ws, world):
         run()
     torch.cuda.synchronize()
     dt = max_over_ranks((time.perf_counter() - t0) / steps, world, dev)
-    return {"value": world * pairs_of(case) / dt, "unit": "pairs/s", "ms_per_step": dt * 1e3,
+    return {"value": sum_over_ranks(pairs_of(case), world, dev) / dt, "unit": "pairs/s",
+            "ms_per_step": dt * 1e3,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
 
 
