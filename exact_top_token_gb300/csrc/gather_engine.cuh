@@ -214,25 +214,32 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
 
     if (warp < 4) {
       // ---------------- producers: gather 128 key rows per tile ----------------
+      // Warp w gathers rows 32w .. 32w+31 of each tile. Lane l fetches the key
+      // index of row 32w + l (two tiles ahead); the copies go CPR lanes per row
+      // (lane l moves 16-byte chunk l % CPR), so that each warp instruction
+      // reads 32 / CPR whole rows.
       const int tid = threadIdx.x;
+      constexpr int RPP = 32 / CPR;  // rows per warp instruction
       int npend = 0;
-      // one row per producer thread; its keys are fetched two tiles ahead
       int s_next = key_of(tid), s_next2 = key_of(kTileKeys + tid);
       for (int i = 0; i < ntiles; ++i) {
-        int s = s_next;
+        int s_own = s_next;
         s_next = s_next2;
         s_next2 = key_of((i + 2) * kTileKeys + tid);
-        if (!tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status)) break;
+        if (s_own >= a.L) s_own = -1;  // stored indices outside [0, L) gather nothing
+        // the warp leaves together (the copies below exchange keys by shuffles)
+        const bool ok = tc::mbar_wait(empty + p_stage, p_phase ^ 1u, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
         uint8_t* dst = ring + p_stage * C_::KT_BYTES;
-        {
-          const int row = tid;
-          if (s >= a.L) s = -1;  // stored indices outside [0, L) gather nothing
-          const uint8_t* src =
-              reinterpret_cast<const uint8_t*>(a.k) + (s >= 0 ? (size_t)s * RB : 0);
+        const int c = lane % CPR;
 #pragma unroll
-          for (int c = 0; c < CPR; ++c)
-            tc::cp_async16(dst + Geo::chunk_offset(row, c, kTileKeys), src + (s >= 0 ? c * 16 : 0),
-                           s >= 0);
+        for (int pass = 0; pass < CPR; ++pass) {
+          const int src_lane = pass * RPP + lane / CPR;
+          const int s = __shfl_sync(0xffffffffu, s_own, src_lane);
+          const int row = warp * 32 + src_lane;
+          const uint8_t* src =
+              reinterpret_cast<const uint8_t*>(a.k) + (s >= 0 ? (size_t)s * RB + c * 16 : 0);
+          tc::cp_async16(dst + Geo::chunk_offset(row, c, kTileKeys), src, s >= 0);
         }
         tc::cp_async_commit();
         ++npend;
