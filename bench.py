@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--workload", default="glm_1m", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-twopass", action="store_true")
+    ap.add_argument("--no-sharded", action="store_true")
+    ap.add_argument("--shards", type=int, default=4, help="key ranges of the sharded selection")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=48, help="oracle sample size (queries)")
     ap.add_argument("--queries", type=int, default=0,
@@ -366,6 +368,8 @@ def gpu_arm(args, world, rank, local):
         line["e2e"] = e2e(args, hk, case, dev, ws, world)
     if not args.no_twopass:
         line["twopass"] = twopass(hk, case, t, dev, idx, pairs)
+    if not args.no_sharded:
+        line["sharded"] = sharded(hk, case, t, dev, idx, pairs, args.shards)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_rows)
     if rank == 0:
@@ -447,6 +451,36 @@ def twopass(hk, case, t, dev, idx_ref, pairs):
     del ws2
     return {"value": pairs / (ms / 1e3), "unit": "pairs/s", "ms": ms, "rows_per_chunk": rows,
             "table_bytes_written": n * L * 4, "same_idx_as_hytopk": same}
+
+
+def sharded(hk, case, t, dev, idx_ref, pairs, P):
+    """The key-sharded selection (one selection per key range + merge), timed
+    once after a warm-up, with its result checked against hytopk_select."""
+    import torch
+
+    n, H, d = case["q"].shape
+    L = case["k"].shape[0]
+    dt_code = hk.E4M3 if case["dtype"] == "e4m3" else hk.BF16
+    ws3 = torch.empty(hk.select_sharded_workspace_size(n, L, H, d, case["k_top"], P, 0, dt_code),
+                      dtype=torch.uint8, device=dev)
+
+    def run():
+        return hk.select_sharded(t["q"], t["k"], t["w"], t["positions"], case["k_top"], P,
+                                 q_scale=t["q_scale"], k_scale=t["k_scale"], workspace=ws3)
+
+    run()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    i3, _, _ = run()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    same = bool(torch.equal(i3, idx_ref))
+    del ws3
+    return {"value": pairs / (ms / 1e3), "unit": "pairs/s", "ms": ms, "shards": P,
+            "same_idx_as_hytopk": same}
 
 
 def main():

@@ -32,6 +32,7 @@ BF16, E4M3 = 0, 1
 # the C-ABI symbols declared in include/hytopk.h
 symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", "hytopk_replay",
            "hytopk_twopass_workspace_size", "hytopk_select_twopass", "hytopk_select_noalloc",
+           "hytopk_select_sharded_workspace_size", "hytopk_select_sharded",
            "hytopk_status_string", "hytopk_version")
 
 
@@ -85,6 +86,11 @@ def load(path: str | None = None):
     lib.hytopk_twopass_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.hytopk_select_twopass.restype = I
     lib.hytopk_select_twopass.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, Z, P, P]
+    lib.hytopk_select_sharded_workspace_size.restype = Z
+    lib.hytopk_select_sharded_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+    lib.hytopk_select_sharded.restype = I
+    lib.hytopk_select_sharded.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, Z, P,
+                                          P]
     lib.hytopk_status_string.restype = ctypes.c_char_p
     lib.hytopk_status_string.argtypes = [I]
     lib.hytopk_version.restype = I
@@ -216,6 +222,36 @@ def select(q, k, w, positions, k_top, *, q_scale=None, k_scale=None, capacity=0,
         ctypes.byref(opts) if opts is not None else None, _stream(dev, stream))
     if status != 0:
         raise HytopkError(status, "hytopk_select")
+    return idx, sc, st
+
+
+def select_sharded_workspace_size(n, L, H, d, k_top, num_shards, capacity=0, dtype=BF16) -> int:
+    return int(load().hytopk_select_sharded_workspace_size(n, L, H, d, k_top, capacity, dtype,
+                                                           num_shards))
+
+
+def select_sharded(q, k, w, positions, k_top, num_shards, *, q_scale=None, k_scale=None,
+                   capacity=0, scores=True, stats=False, workspace=None, stream=None):
+    """Key-sharded exact selection: one HyTopK selection per key range, then a
+    merge per query. Same outputs as :func:`select`."""
+    import torch
+
+    lib = load()
+    dt, n, L, H, d, dev = _common(q, q_scale, k, k_scale, w)
+    _check_tensor("positions", positions, dev, torch.int32, (n,))
+    idx = torch.empty((n, k_top), dtype=torch.int32, device=dev)
+    sc = torch.empty((n, k_top), dtype=torch.float32, device=dev) if scores else None
+    need = lib.hytopk_select_sharded_workspace_size(n, L, H, d, k_top, capacity, dt, num_shards)
+    if need == 0:
+        raise HytopkError(2, "hytopk_select_sharded_workspace_size")
+    ws = _workspace(need, dev, workspace)
+    st = torch.zeros(8, dtype=torch.int32, device=dev) if stats else None
+    status = lib.hytopk_select_sharded(
+        _ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(positions), n, L, H, d,
+        k_top, dt, num_shards, _ptr(idx), _ptr(sc), capacity, _ptr(ws), ws.numel(), _ptr(st),
+        _stream(dev, stream))
+    if status != 0:
+        raise HytopkError(status, "hytopk_select_sharded")
     return idx, sc, st
 
 

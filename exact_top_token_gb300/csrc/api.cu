@@ -20,29 +20,6 @@ int elem_size(hytopk_dtype dt) { return dt == HYTOPK_BF16 ? 2 : 1; }
 bool valid_dtype(hytopk_dtype dt) { return dt == HYTOPK_BF16 || dt == HYTOPK_E4M3; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Shape checks shared by every entry point.
-hytopk_status check_shape(int n, int L, int H, int d, int k_top, hytopk_dtype dt) {
-  if (n < 0 || L < 1 || H < 1 || d < 1 || k_top < 1 || !valid_dtype(dt)) return HYTOPK_INVALID_ARG;
-  if (!supported_h(H) || !supported_d(d) || k_top > kMaxTopK) return HYTOPK_UNSUPPORTED;
-  if (n > (1 << 22) || L > (1 << 30)) return HYTOPK_UNSUPPORTED;
-  return HYTOPK_OK;
-}
-
-hytopk_status check_inputs(const void* q, const float* q_scale, const void* k, const float* k_scale,
-                           const float* w, hytopk_dtype dt, int n) {
-  if (!k) return HYTOPK_INVALID_ARG;
-  if (n > 0 && (!q || !w)) return HYTOPK_INVALID_ARG;
-  if (dt == HYTOPK_E4M3) {
-    if (!k_scale || (n > 0 && !q_scale)) return HYTOPK_INVALID_ARG;
-  } else if (q_scale || k_scale) {
-    return HYTOPK_INVALID_ARG;
-  }
-  const void* ptrs[] = {q, q_scale, k, k_scale, w};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return HYTOPK_MISALIGNED;
-  return HYTOPK_OK;
-}
-
 int pad_queries(int n) { return (n + kQueryPad - 1) / kQueryPad * kQueryPad; }
 
 struct SelectLayout {
@@ -109,6 +86,33 @@ hytopk_status record(const hytopk_select_options* opts, int phase, cudaStream_t 
 }
 
 }  // namespace
+
+namespace hytopk {
+
+// Shape checks shared by every entry point.
+hytopk_status check_shape(int n, int L, int H, int d, int k_top, hytopk_dtype dt) {
+  if (n < 0 || L < 1 || H < 1 || d < 1 || k_top < 1 || !valid_dtype(dt)) return HYTOPK_INVALID_ARG;
+  if (!supported_h(H) || !supported_d(d) || k_top > kMaxTopK) return HYTOPK_UNSUPPORTED;
+  if (n > (1 << 22) || L > (1 << 30)) return HYTOPK_UNSUPPORTED;
+  return HYTOPK_OK;
+}
+
+hytopk_status check_inputs(const void* q, const float* q_scale, const void* k, const float* k_scale,
+                           const float* w, hytopk_dtype dt, int n) {
+  if (!k) return HYTOPK_INVALID_ARG;
+  if (n > 0 && (!q || !w)) return HYTOPK_INVALID_ARG;
+  if (dt == HYTOPK_E4M3) {
+    if (!k_scale || (n > 0 && !q_scale)) return HYTOPK_INVALID_ARG;
+  } else if (q_scale || k_scale) {
+    return HYTOPK_INVALID_ARG;
+  }
+  const void* ptrs[] = {q, q_scale, k, k_scale, w};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return HYTOPK_MISALIGNED;
+  return HYTOPK_OK;
+}
+
+}  // namespace hytopk
 
 extern "C" {
 

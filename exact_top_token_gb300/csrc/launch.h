@@ -43,4 +43,9 @@ cudaError_t launch_plan(const SelectWs& ws, int L, int qb, cudaStream_t st);
 // Shared-memory bytes of the candidate selection for k_top.
 size_t select_smem_bytes(int k_top);
 
+// Host-side argument checks shared by the entry points (api.cu).
+hytopk_status check_shape(int n, int L, int H, int d, int k_top, hytopk_dtype dt);
+hytopk_status check_inputs(const void* q, const float* q_scale, const void* k,
+                           const float* k_scale, const float* w, hytopk_dtype dt, int n);
+
 }  // namespace hytopk

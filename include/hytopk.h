@@ -224,6 +224,38 @@ hytopk_status hytopk_select_noalloc(const void* q, const float* q_scale, const v
                                     float* scores_out, int capacity, hytopk_stats* stats_out,
                                     cudaStream_t stream);
 
+/* Key-sharded exact selection: the single-GPU stand-in for selection under
+ * context parallelism, where each GPU holds one range of the keys (Summary,
+ * "What the paper found", and Explainer, limits paragraph: context-parallel
+ * communication overlapped with selection; the pages do not describe how a
+ * sharded selection is combined).
+ *   The keys [0, L) are split into ranges of S = ceil(L / num_shards) keys
+ *   rounded up to a multiple of 128; range p is [p*S, min(L, (p+1)*S)).
+ *   For each range, in turn, hytopk_select runs over that range alone (its
+ *   own sampled threshold, filter, check and recovery), giving each query the
+ *   exact top-k of its causal keys inside the range (none if its position is
+ *   below the range). Then one merge per query keeps the exact top-k of the
+ *   union of those lists, with the same order and tie rule (score
+ *   descending, then lower global position). The result equals hytopk_select
+ *   bit for bit: under one total order the k best of a union are among the k
+ *   best of each part.
+ *   num_shards: 1 .. 64. Ranges that start at or after L are skipped.
+ *   workspace: hytopk_select_sharded_workspace_size bytes, 256-byte aligned.
+ *   stats_out: device hytopk_stats or NULL; counts are summed over the
+ *   ranges (a query can fail in several), fallback_used is set if any range
+ *   fell back, device_status ORs the ranges' bits, n_queries = n.
+ * Other arguments, outputs and errors are those of hytopk_select. */
+size_t hytopk_select_sharded_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
+                                            hytopk_dtype dt, int num_shards);
+
+hytopk_status hytopk_select_sharded(const void* q, const float* q_scale, const void* k,
+                                    const float* k_scale, const float* w,
+                                    const int32_t* positions, int n, int L, int H, int d,
+                                    int k_top, hytopk_dtype dt, int num_shards, int32_t* idx_out,
+                                    float* scores_out, int capacity, void* workspace,
+                                    size_t workspace_bytes, hytopk_stats* stats_out,
+                                    cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* hytopk_status_string(hytopk_status status);
 

@@ -31,7 +31,9 @@ def main():
            "pairs_all": bench.sum_over_ranks(pairs, world, cpu),
            "ms_max": bench.max_over_ranks(fake_ms, world, cpu)}
     bench.barrier(world)
-    print("RESULT " + json.dumps(out), flush=True)
+    # one file per rank (the ranks share one stdout, where lines can interleave)
+    with open(os.path.join(sys.argv[1], f"rank{rank}.json"), "w") as f:
+        json.dump(out, f)
     dist.destroy_process_group()
 
 

@@ -80,3 +80,34 @@ def test_host_checks_reject_bad_arguments(lib):
     assert r == 1  # idx missing
     assert lib.hytopk_select_twopass(fake, None, fake, None, fake, fake, 4, 100, 4, 64, 8, 0, fake,
                                      None, fake, 16, None, None) == 3
+
+
+def test_sharded_host_checks(lib):
+    ws = lib.hytopk_select_sharded_workspace_size
+    one = lib.hytopk_select_workspace_size(64, 4096, 4, 64, 256, 0, 0)
+    assert ws(64, 4096, 4, 64, 256, 0, 0, 1) > one  # + local lists and merge keys
+    assert ws(64, 4096, 4, 64, 256, 0, 0, 0) == 0  # no shard
+    assert ws(64, 4096, 4, 64, 256, 0, 0, 65) == 0  # more than 64 shards
+    assert ws(64, 4096, 3, 64, 256, 0, 0, 2) == 0  # H not a power of two
+    # one range's selection workspace (512 keys) + the merge keys, n x P x k x 8 bytes
+    assert ws(64, 4096, 4, 64, 256, 0, 0, 8) >= \
+        lib.hytopk_select_workspace_size(64, 512, 4, 64, 256, 0, 0) + 64 * 8 * 256 * 8
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def call(**kw):
+        a = dict(q=fake, qs=None, k=fake, ks=None, w=fake, pos=fake, n=4, L=100, H=4, d=64,
+                 k_top=8, dt=0, P=2, idx=fake, sc=None, cap=0, ws=fake, wsb=1 << 30, st=None)
+        a.update(kw)
+        return lib.hytopk_select_sharded(a["q"], a["qs"], a["k"], a["ks"], a["w"], a["pos"],
+                                         a["n"], a["L"], a["H"], a["d"], a["k_top"], a["dt"],
+                                         a["P"], a["idx"], a["sc"], a["cap"], a["ws"], a["wsb"],
+                                         a["st"], None)
+
+    assert call(P=0) == 1
+    assert call(P=100) == 1
+    assert call(H=6) == 2
+    assert call(k=None) == 1
+    assert call(wsb=16) == 3
+    assert call(ws=P((1 << 20) + 128)) == 5
+    assert call(pos=None) == 1

@@ -50,11 +50,10 @@ def test_shard_case_keeps_other_workloads():
         assert np.array_equal(bench.shard_case(case, 2, r)["positions"], case["positions"])
 
 
-def test_two_gloo_ranks_reduce_times_and_pairs():
-    r = torchrun([os.path.join("tests", "dist_worker.py")])
+def test_two_gloo_ranks_reduce_times_and_pairs(tmp_path):
+    r = torchrun([os.path.join("tests", "dist_worker.py"), str(tmp_path)])
     assert r.returncode == 0, r.stderr[-3000:]
-    res = [json.loads(l[len("RESULT "):]) for l in r.stdout.splitlines()
-           if l.startswith("RESULT ")]
+    res = [json.load(open(tmp_path / f"rank{i}.json")) for i in range(2)]
     assert sorted(x["rank"] for x in res) == [0, 1]
     by_rank = {x["rank"]: x for x in res}
     total = by_rank[0]["pairs"] + by_rank[1]["pairs"]
