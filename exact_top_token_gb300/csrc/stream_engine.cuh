@@ -258,6 +258,50 @@ __device__ __forceinline__ void flush_staged(int block, uint32_t* scnt, const ui
     if (lane == 0) scnt[jb] = 0;
 }
 
+// Private staging, for warps that serve at most a few queries of the block:
+// the (query, lane quadrant) pair owns a region of CAP / 4 entries and the warp
+// keeps its fill level in a register, so an append needs no atomic at all.
+template <int CAP4>
+__device__ __forceinline__ void append_private(bool pass, float score, int s, int region, int slot,
+                                               uint32_t& fill, uint64_t* stage, int32_t* cnt,
+                                               uint64_t* cand, int C) {
+  const unsigned mask = __ballot_sync(0xffffffffu, pass);
+  if (mask == 0u) return;
+  const int lane = threadIdx.x & 31;
+  if (pass) {
+    const uint32_t at = fill + (uint32_t)__popc(mask & ((1u << lane) - 1u));
+    const uint64_t key = cand_key(score, s);
+    if (at < (uint32_t)CAP4) {
+      stage[region * CAP4 + at] = key;
+    } else {
+      const int g = atomicAdd(cnt + slot, 1);
+      if (g < C) cand[(size_t)slot * C + g] = key;
+    }
+  }
+  fill += (uint32_t)__popc(mask);
+}
+
+// Move one private region to the query's global buffer (one atomic) and
+// empty it; the whole warp calls it.
+template <int CAP4>
+__device__ __forceinline__ void flush_private(int region, int slot, uint32_t& fill,
+                                              const uint64_t* stage, int32_t* cnt, uint64_t* cand,
+                                              int C) {
+  const uint32_t n = min(fill, (uint32_t)CAP4);
+  fill = 0;
+  if (n == 0) return;
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  int base = 0;
+  if (lane == 0) base = atomicAdd(cnt + slot, (int)n);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  for (uint32_t i = lane; i < n; i += 32) {
+    const int g = base + (int)i;
+    if (g < C) cand[(size_t)slot * C + g] = stage[region * CAP4 + i];
+  }
+  __syncwarp();
+}
+
 template <int D, int DT, int H, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_stream(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
@@ -457,12 +501,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t aphase = 0;
     int prev_block = -1;
-    if (MODE == 0)
+    // candidate staging: private regions (REG_META) or shared counters
+    constexpr int CAP4 = CAP / 4;
+    uint32_t fill[REG_META ? NQS : 1];
+    if constexpr (REG_META) {
+#pragma unroll
+      for (int u = 0; u < NQS; ++u) fill[u] = 0;
+    }
+    if (MODE == 0 && !REG_META)
       for (int jb = et; jb < QB; jb += kEpiWarps * 32) scnt_s[jb] = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x) {
       const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
       epi_sync();
-      if (MODE == 0 && prev_block >= 0)
+      if (MODE == 0 && !REG_META && prev_block >= 0)
         flush_staged<QB, CAP>(prev_block, scnt_s, stage_s, a.cnt, a.cand, a.C, e);
       prev_block = itm.block;
       for (int jb = et; jb < QB; jb += kEpiWarps * 32) {
@@ -585,8 +636,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if (MODE == 0) {
                 const bool pass = (s <= p) && (sc >= thr);
-                append_staged<CAP>(pass, sc, s, qlo + qi, rrow[qi], scnt_s, stage_s, a.cnt,
-                                   a.cand, a.C);
+                if constexpr (REG_META)
+                  append_private<CAP4>(pass, sc, s, (qlo + qi) * 4 + quad, rrow[qi], fill[qi],
+                                       stage_s, a.cnt, a.cand, a.C);
+                else
+                  append_staged<CAP>(pass, sc, s, qlo + qi, rrow[qi], scnt_s, stage_s, a.cnt,
+                                     a.cand, a.C);
               } else {
                 const int r = rrow[qi];
                 if (r >= 0 && s < a.L)
@@ -607,8 +662,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc ^= 1;
         if (acc == 0) aphase ^= 1u;
       }
+      if constexpr (MODE == 0 && REG_META) {
+#pragma unroll
+        for (int u = 0; u < NQS; ++u)
+          flush_private<CAP4>((qlo + u) * 4 + quad, rrow[u], fill[u], stage_s, a.cnt, a.cand,
+                              a.C);
+      }
     }
-    if (MODE == 0) {
+    if (MODE == 0 && !REG_META) {
       epi_sync();
       if (prev_block >= 0)
         flush_staged<QB, CAP>(prev_block, scnt_s, stage_s, a.cnt, a.cand, a.C, e);
