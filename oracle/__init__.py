@@ -72,6 +72,9 @@ def _load():
     lib.oracle_select.argtypes = common + [P, P, I64, I64, I64, I32, I32, I32, I64, P, P, I32]
     lib.oracle_replay.restype = I32
     lib.oracle_replay.argtypes = common + [P, I64, I64, I32, I32, I32, I64, P, P, I32]
+    lib.oracle_backward.restype = I32
+    lib.oracle_backward.argtypes = common + [P, P, I64, I64, I32, I32, I32, I64,
+                                             ctypes.c_double] + [P] * 10 + [I32]
     lib.oracle_filter_sim.restype = I32
     lib.oracle_filter_sim.argtypes = common + [
         P, P, I64, I64, I64, I32, I32, I32, I64, I64, P, P, P, P, P, I32]
@@ -202,6 +205,29 @@ def replay(inp, idx, nthreads: int = 0):
                                nthreads)
     _check(st, "replay")
     return out, int(bad[0])
+
+
+def backward(inp, idx, grad, eps: float = 0.0, nthreads: int = 0):
+    """Gradients of sum_{t,j} grad[t,j] * I[t, idx[t,j]] (fp64): a dict with
+    dq [n,H,d], dk [L,d], dw [n,H], the matching *_abs (sum of |terms|) and
+    *_amb (|terms| whose head dot is within eps*|q||k| of zero), and bad (the
+    number of indices outside [0, L) other than -1)."""
+    keep, args, pos, n, L, H, d, dt = _prep(inp)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    grad = np.ascontiguousarray(grad, dtype=np.float32)
+    k_top = idx.shape[1]
+    out = {name: np.zeros(shape, dtype=np.float64) for name, shape in (
+        ("dq", (n, H, d)), ("dk", (L, d)), ("dw", (n, H)), ("dq_abs", (n, H, d)),
+        ("dk_abs", (L, d)), ("dw_abs", (n, H)), ("dq_amb", (n, H, d)), ("dk_amb", (L, d)),
+        ("dw_amb", (n, H)))}
+    bad = np.zeros(1, dtype=np.int64)
+    st = _load().oracle_backward(
+        *args, _ptr(idx), _ptr(grad), n, L, H, d, dt, k_top, float(eps),
+        *[_ptr(out[k]) for k in ("dq", "dk", "dw", "dq_abs", "dk_abs", "dw_abs", "dq_amb",
+                                 "dk_amb", "dw_amb")], _ptr(bad), nthreads)
+    _check(st, "backward")
+    out["bad"] = int(bad[0])
+    return out
 
 
 def filter_sim(inp, capacity: int, rows=None, nthreads: int = 0):

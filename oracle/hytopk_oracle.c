@@ -46,6 +46,17 @@
  *   Replay (Explainer, selection replay paragraph): the same score at stored
  *     indices; index -1 gives -inf, any other index outside [0, L) gives NaN
  *     and is counted as bad.
+ *   Backward at the selected entries (Explainer, key-observation paragraph:
+ *     the indexer's own loss reads only the scores at the selected entries;
+ *     selection-replay paragraph: those entries are rescored during
+ *     recomputation). Given G[t,j] = dLoss/dI[t, idx[t,j]] (READING: the loss
+ *     itself is not on the pages, so its gradient is an input), with the
+ *     dequantised inputs qd = q*q_scale and kd = k*k_scale, x = qd[t,h].kd[s]:
+ *       dw[t,h]   = sum_j G[t,j] * max(0, x[t,h,idx[t,j]])
+ *       dq[t,h,:] = sum_j G[t,j] * w[t,h] * [x > 0] * kd[idx[t,j],:]
+ *       dk[s,:]  += sum_{(t,j): idx[t,j] = s} G[t,j] * sum_h w[t,h] * [x > 0] * qd[t,h,:]
+ *     READING: the derivative of max(0, x) at x = 0 is taken as 0. This part
+ *     is computed in fp64 (the pages fix no precision for it).
  */
 #include <math.h>
 #include <stdint.h>
@@ -398,4 +409,147 @@ int oracle_filter_sim(const void* q, const float* q_scale, const void* k, const 
   }
   free(p.kf);
   return ORACLE_OK;
+}
+
+/* Backward of sum_{t,j} G[t,j] * I[t, idx[t,j]] (see the header): outputs in
+ * fp64, dq [n,H,d] and dw [n,H] written, dk [L,d] accumulated into. For
+ * tolerances it also returns, per output element, the sum of the absolute
+ * values of its terms (*_abs) and the part of that sum whose head dot x lies
+ * within eps * |qd[t,h]| * |kd[s]| of zero (*_amb: terms whose [x > 0]
+ * depends on rounding). Any of the *_abs / *_amb arrays may be NULL.
+ * Entries with idx = -1 contribute nothing; other indices outside [0, L) are
+ * counted in *bad and skipped. */
+int oracle_backward(const void* q, const float* q_scale, const void* k, const float* k_scale,
+                    const float* w, const int32_t* idx, const float* grad, int64_t n, int64_t L,
+                    int H, int d, int dtype, int64_t k_top, double eps, double* dq, double* dk,
+                    double* dw, double* dq_abs, double* dk_abs, double* dw_abs, double* dq_amb,
+                    double* dk_amb, double* dw_amb, int64_t* bad, int nthreads) {
+  if (n < 0 || L <= 0 || H <= 0 || d <= 0 || k_top <= 0) return ORACLE_BAD_ARG;
+  if (dtype != ORACLE_BF16 && dtype != ORACLE_E4M3) return ORACLE_BAD_ARG;
+  if (dtype == ORACLE_E4M3 && (!q_scale || !k_scale)) return ORACLE_BAD_ARG;
+  const size_t Hd = (size_t)H * d;
+  /* dequantised keys and their norms, fp64 (the products are exact) */
+  double* kd = (double*)malloc((size_t)L * d * sizeof(double));
+  double* knorm = (double*)malloc((size_t)L * sizeof(double));
+  if (!kd || !knorm) {
+    free(kd);
+    free(knorm);
+    return ORACLE_NO_MEMORY;
+  }
+  set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+  for (int64_t s = 0; s < L; ++s) {
+    double scale = dtype == ORACLE_E4M3 ? (double)k_scale[s] : 1.0;
+    double nn = 0.0;
+    for (int i = 0; i < d; ++i) {
+      double v = (double)element(k, dtype, (size_t)s * d + i) * scale;
+      kd[(size_t)s * d + i] = v;
+      nn += v * v;
+    }
+    knorm[s] = sqrt(nn);
+  }
+  int64_t nbad = 0;
+  for (int64_t t = 0; t < n; ++t)
+    for (int64_t j = 0; j < k_top; ++j) {
+      int32_t s = idx[t * k_top + j];
+      if (s != -1 && (s < 0 || s >= L)) ++nbad;
+    }
+  /* dq and dw: one query at a time (independent) */
+#pragma omp parallel
+  {
+    double* qd = (double*)malloc(Hd * sizeof(double));
+    double* qnorm = (double*)malloc((size_t)H * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t t = 0; t < n; ++t) {
+      for (int h = 0; h < H; ++h) {
+        double scale = dtype == ORACLE_E4M3 ? (double)q_scale[t * H + h] : 1.0;
+        double nn = 0.0;
+        for (int i = 0; i < d; ++i) {
+          double v = (double)element(q, dtype, ((size_t)t * H + h) * d + i) * scale;
+          qd[(size_t)h * d + i] = v;
+          nn += v * v;
+        }
+        qnorm[h] = sqrt(nn);
+      }
+      double* dqt = dq + (size_t)t * Hd;
+      for (size_t e = 0; e < Hd; ++e) {
+        dqt[e] = 0.0;
+        if (dq_abs) dq_abs[(size_t)t * Hd + e] = 0.0;
+        if (dq_amb) dq_amb[(size_t)t * Hd + e] = 0.0;
+      }
+      for (int h = 0; h < H; ++h) {
+        dw[t * H + h] = 0.0;
+        if (dw_abs) dw_abs[t * H + h] = 0.0;
+        if (dw_amb) dw_amb[t * H + h] = 0.0;
+      }
+      for (int64_t j = 0; j < k_top; ++j) {
+        int32_t s = idx[t * k_top + j];
+        if (s < 0 || s >= L) continue;
+        double g = (double)grad[t * k_top + j];
+        const double* ks = kd + (size_t)s * d;
+        for (int h = 0; h < H; ++h) {
+          double x = 0.0;
+          for (int i = 0; i < d; ++i) x += qd[(size_t)h * d + i] * ks[i];
+          int amb = fabs(x) <= eps * qnorm[h] * knorm[s];
+          double relu = x > 0.0 ? x : 0.0;
+          dw[t * H + h] += g * relu;
+          if (dw_abs) dw_abs[t * H + h] += fabs(g * relu);
+          if (dw_amb && amb) dw_amb[t * H + h] += fabs(g * x);
+          double coef = g * (double)w[t * H + h];
+          for (int i = 0; i < d; ++i) {
+            size_t e = (size_t)h * d + i;
+            if (x > 0.0) {
+              dqt[e] += coef * ks[i];
+              if (dq_abs) dq_abs[(size_t)t * Hd + e] += fabs(coef * ks[i]);
+            }
+            if (dq_amb && amb) dq_amb[(size_t)t * Hd + e] += fabs(coef * ks[i]);
+          }
+        }
+      }
+    }
+    free(qnorm);
+    free(qd);
+  }
+  /* dk: every (query, entry) adds into its key's row, in query order */
+  double* qd = (double*)malloc(Hd * sizeof(double));
+  double* qnorm = (double*)malloc((size_t)H * sizeof(double));
+  for (int64_t t = 0; t < n && qd && qnorm; ++t) {
+    for (int h = 0; h < H; ++h) {
+      double scale = dtype == ORACLE_E4M3 ? (double)q_scale[t * H + h] : 1.0;
+      double nn = 0.0;
+      for (int i = 0; i < d; ++i) {
+        double v = (double)element(q, dtype, ((size_t)t * H + h) * d + i) * scale;
+        qd[(size_t)h * d + i] = v;
+        nn += v * v;
+      }
+      qnorm[h] = sqrt(nn);
+    }
+    for (int64_t j = 0; j < k_top; ++j) {
+      int32_t s = idx[t * k_top + j];
+      if (s < 0 || s >= L) continue;
+      double g = (double)grad[t * k_top + j];
+      const double* ks = kd + (size_t)s * d;
+      for (int h = 0; h < H; ++h) {
+        double x = 0.0;
+        for (int i = 0; i < d; ++i) x += qd[(size_t)h * d + i] * ks[i];
+        int amb = fabs(x) <= eps * qnorm[h] * knorm[s];
+        double coef = g * (double)w[t * H + h];
+        for (int i = 0; i < d; ++i) {
+          size_t e = (size_t)s * d + i;
+          if (x > 0.0) {
+            dk[e] += coef * qd[(size_t)h * d + i];
+            if (dk_abs) dk_abs[e] += fabs(coef * qd[(size_t)h * d + i]);
+          }
+          if (dk_amb && amb) dk_amb[e] += fabs(coef * qd[(size_t)h * d + i]);
+        }
+      }
+    }
+  }
+  int st = (qd && qnorm) ? ORACLE_OK : ORACLE_NO_MEMORY;
+  free(qnorm);
+  free(qd);
+  free(knorm);
+  free(kd);
+  if (bad) *bad = nbad;
+  return st;
 }

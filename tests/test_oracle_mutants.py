@@ -8,6 +8,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_backward as bpins
 import test_oracle_pins as pins
 
 MUTANTS = [
@@ -34,6 +35,16 @@ MUTANTS = [
     ("sample_midpoint", "return (j * ctx) / m;", "return (j * ctx + ctx / 2) / m;"),
     ("subnormal_exp", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     ("e4m3_bias", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    # the backward at selected entries
+    ("bwd_dq_no_weight", "dqt[e] += coef * ks[i];", "dqt[e] += g * ks[i];"),
+    ("bwd_dk_uses_key", "dk[e] += coef * qd[(size_t)h * d + i];", "dk[e] += coef * ks[i];"),
+    ("bwd_dw_no_relu", "dw[t * H + h] += g * relu;", "dw[t * H + h] += g * x;"),
+    ("bwd_mask_at_zero", "if (x > 0.0) {\n              dqt[e]", "if (x >= 0.0) {\n              dqt[e]"),
+    ("bwd_wrong_key_row", "size_t e = (size_t)s * d + i;", "size_t e = (size_t)((s + 1) % L) * d + i;"),
+    ("bwd_no_k_scale", "double v = (double)element(k, dtype, (size_t)s * d + i) * scale;",
+     "double v = (double)element(k, dtype, (size_t)s * d + i);"),
+    ("bwd_grad_row", "double g = (double)grad[t * k_top + j];\n        const double* ks = kd + (size_t)s * d;\n        for (int h = 0; h < H; ++h) {\n          double x = 0.0;\n          for (int i = 0; i < d; ++i) x += qd[(size_t)h * d + i] * ks[i];\n          int amb = fabs(x) <= eps * qnorm[h] * knorm[s];\n          double relu",
+     "double g = (double)grad[((t + 1) % n) * k_top + j];\n        const double* ks = kd + (size_t)s * d;\n        for (int h = 0; h < H; ++h) {\n          double x = 0.0;\n          for (int i = 0; i < d; ++i) x += qd[(size_t)h * d + i] * ks[i];\n          int amb = fabs(x) <= eps * qnorm[h] * knorm[s];\n          double relu"),
 ]
 
 
@@ -54,6 +65,12 @@ def battery():
         pins.test_filter_full_sampling_threshold_is_exact_rank,
         pins.test_filter_certificate_holds,
         pins.test_filter_threshold_rank_on_distinct_scores,
+        bpins.test_dw_is_the_difference_in_w,
+        bpins.test_dq_is_the_difference_in_q,
+        bpins.test_dk_is_the_difference_in_k,
+        bpins.test_relu_kink_derivative_is_zero,
+        bpins.test_empty_and_bad_indices,
+        bpins.test_e4m3_scales_enter_the_gradient,
     ]
     failed = 0
     for check in checks:
