@@ -33,6 +33,7 @@ BF16, E4M3 = 0, 1
 symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", "hytopk_replay",
            "hytopk_twopass_workspace_size", "hytopk_select_twopass", "hytopk_select_noalloc",
            "hytopk_select_sharded_workspace_size", "hytopk_select_sharded",
+           "hytopk_replay_backward",
            "hytopk_status_string", "hytopk_version")
 
 
@@ -91,6 +92,8 @@ def load(path: str | None = None):
     lib.hytopk_select_sharded.restype = I
     lib.hytopk_select_sharded.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, I, P, Z, P,
                                           P]
+    lib.hytopk_replay_backward.restype = I
+    lib.hytopk_replay_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]
     lib.hytopk_status_string.restype = ctypes.c_char_p
     lib.hytopk_status_string.argtypes = [I]
     lib.hytopk_version.restype = I
@@ -276,6 +279,31 @@ def replay(q, k, w, idx, *, q_scale=None, k_scale=None, status=None, out=None, s
     if st != 0:
         raise HytopkError(st, "hytopk_replay")
     return res
+
+
+def replay_backward(q, k, w, idx, grad, *, q_scale=None, k_scale=None, dk=None, status=None,
+                    stream=None):
+    """Gradients at the selected entries: returns (dq [n,H,d], dk [L,d], dw [n,H]),
+    fp32. ``dk`` is added to when given (else a zeroed tensor is used)."""
+    import torch
+
+    lib = load()
+    dt, n, L, H, d, dev = _common(q, q_scale, k, k_scale, w)
+    k_top = idx.shape[1]
+    _check_tensor("idx", idx, dev, torch.int32, (n, k_top))
+    _check_tensor("grad", grad, dev, torch.float32, (n, k_top))
+    dq = torch.empty((n, H, d), dtype=torch.float32, device=dev)
+    dw = torch.empty((n, H), dtype=torch.float32, device=dev)
+    if dk is None:
+        dk = torch.zeros((L, d), dtype=torch.float32, device=dev)
+    else:
+        _check_tensor("dk", dk, dev, torch.float32, (L, d))
+    st = lib.hytopk_replay_backward(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w),
+                                    _ptr(idx), _ptr(grad), n, L, H, d, k_top, dt, _ptr(dq),
+                                    _ptr(dk), _ptr(dw), _ptr(status), _stream(dev, stream))
+    if st != 0:
+        raise HytopkError(st, "hytopk_replay_backward")
+    return dq, dk, dw
 
 
 def select_twopass(q, k, w, positions, k_top, *, q_scale=None, k_scale=None, rows_per_chunk=0,

@@ -1,0 +1,618 @@
+// backward_engine.cuh -- gradients of the indexer score at the selected
+// entries: for every query t and stored index s = idx[t,j] with upstream
+// gradient G = grad[t,j] (dLoss/dI[t,s]),
+//   dw[t,h]   = sum_j G * max(0, x)
+//   dq[t,h,:] = sum_j G * w[t,h] * [x > 0] * kd[s,:]
+//   dk[s,:]  += G * sum_h w[t,h] * [x > 0] * qd[t,h,:]
+// with qd = q * q_scale, kd = k * k_scale and x = qd[t,h] . kd[s].
+//
+// HyScale explainer, key-observation paragraph (the indexer's own loss reads
+// only the scores at the selected entries) and selection-replay paragraph
+// (during recomputation only those entries are rescored): this is that
+// rescoring, fused with the gradient it exists for. The loss is not on the
+// pages; its gradient at the entries is the input. The derivative of max(0,x)
+// at x = 0 is taken as 0.
+//
+// Per query (one CTA per SM, queries blockIdx.x, +gridDim.x, ...) and per tile
+// of 128 stored keys:
+//   producers (warps 0-3): gather the 128 key rows into shared memory as bf16
+//     (e4m3 codes convert exactly), 128-byte swizzle, 8 lanes per row;
+//     at a query's start also its q rows (bf16) and its w and q_scale.
+//   MMA issuer (warp 4), all kind::f16 with bf16 operands, fp32 accumulate:
+//     X   [128 keys x H]  = Kt . Q^T            (keys K-major, q K-major)
+//     DQ  [2H x d]       += Aq^T . Kt           (Aq MN-major, keys MN-major),
+//         accumulated over the query's tiles
+//     DK  [128 keys x d]  = Ak . Q              (Ak K-major, q MN-major)
+//   epilogue (warps 8-11, TMEM lane = key): from its row of X, E[h] = G w[h]
+//     [X[h] > 0]; writes Aq[key][h'] = E[h] * k_scale and Ak[key][h'] =
+//     E[h] * q_scale[h], each split into a bf16 high part (h' = h) and the
+//     bf16 of the remainder (h' = H + h), so the products carry ~16 bits;
+//     sums G k_scale max(0, X[h]) over keys with warp butterflies (dw); adds
+//     its DK row into dk[s] with vector reductions; at the query's end adds the
+//     high and low DQ rows and writes dq[t], and writes dw[t].
+// The raw dot X uses the unscaled codes; scales are > 0, so [x > 0] =
+// [X > 0] and max(0, x) = k_scale * q_scale * max(0, X).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tc.cuh"
+
+namespace hytopk {
+namespace bwd {
+
+constexpr int kThreads = 384;
+constexpr int kProducers = 128;
+constexpr int kMmaWarp = 4;
+constexpr int kTmemWarp = 5;
+constexpr int kEpiFirstWarp = 8;
+
+struct BArgs {
+  const void* q;
+  const float* q_scale;
+  const void* k;
+  const float* k_scale;
+  const float* w;
+  const int32_t* idx;
+  const float* grad;
+  float* dq;
+  float* dk;
+  float* dw;
+  int n, L, k_top;
+  uint32_t* status;
+};
+
+template <int D, int DT, int H>
+struct Cfg {
+  static constexpr int ES = DT == 0 ? 2 : 1;  // input element bytes
+  static constexpr int RB = D * 2;            // bf16 row bytes in shared memory
+  static constexpr int DA = RB / 128;         // 128-byte atoms per bf16 row
+  static constexpr int STAGES = 3;
+  static constexpr int KT = 128 * RB;        // bf16 key tile
+  static constexpr int QT = H * RB;          // bf16 q operand of one query
+  static constexpr int AT = 128 * 256;       // Aq / Ak: 128 keys x 128 bf16
+  static constexpr int RING_OFF = 0;
+  static constexpr int Q_OFF = RING_OFF + STAGES * KT;
+  static constexpr int AQ_OFF = Q_OFF + 2 * ((QT + 1023) / 1024 * 1024);
+  static constexpr int AK_OFF = AQ_OFF + AT;
+  static constexpr int WS_OFF = AK_OFF + AT;          // w, q_scale: [2][2][H] fp32
+  static constexpr int DWS_OFF = WS_OFF + 2 * 2 * H * 4;  // dw partials [4][H]
+  static constexpr int BAR_OFF = DWS_OFF + 4 * H * 4;
+  // k_full[S], k_empty[S], q_full[2], q_empty[2], x_full[2], x_empty[2],
+  // a_full, a_empty, dk_full[2], dk_empty[2], dq_full, dq_empty, epilogue meet
+  static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1 + 1 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
+  static constexpr int SMEM = MISC_OFF + 16 + 1024;
+  // TMEM columns
+  static constexpr int X_COL = 0;           // 2 buffers of H
+  static constexpr int DQ_COL = 128;        // d columns
+  static constexpr int DK_COL = 256;        // 2 buffers of d
+  static constexpr int CPRS = D * ES / 16;  // 16-byte source chunks per key row
+  static_assert(H == 16 || H == 32 || H == 64, "H");
+  static_assert(D == 64 || D == 128, "d");
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+// Byte offset of bf16 element e of row r in a 128-byte-swizzled tile whose
+// rows hold `rb` bytes, laid out as [atom][rows][128 B] (rows a multiple of 8).
+__device__ __forceinline__ uint32_t sw_off(int r, int e, int rows) {
+  const int atom = e >> 6;
+  const int c = (e & 63) >> 3;
+  return (uint32_t)(atom * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 +
+                    ((c ^ (r & 7)) << 4) + (e & 7) * 2);
+}
+
+// Shared-memory descriptor with both byte offsets (SW128).
+__device__ __forceinline__ uint64_t desc2(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
+}
+
+// 16 e4m3 codes -> 16 bf16 (exact: every e4m3 value is a bf16 value).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 in, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t out[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const uint16_t two = (uint16_t)(w[i] >> (16 * p));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+      const float f0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+      const float f1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+      uint32_t b2;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(f1), "f"(f0));
+      out[2 * i + p] = b2;
+    }
+  }
+  lo = make_uint4(out[0], out[1], out[2], out[3]);
+  hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+// high bf16 part of v and the bf16 of the remainder, as raw bits
+__device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  const __nv_bfloat16 l = __float2bfloat16_rn(v - __bfloat162float(h));
+  hi = __bfloat16_as_ushort(h);
+  lo = __bfloat16_as_ushort(l);
+}
+
+// The four epilogue warps meet on an mbarrier (count 128) rather than a named
+// barrier, so that a wait that gives up cannot leave the others waiting
+// forever.
+__device__ __forceinline__ bool epi_meet(uint64_t* bar, uint32_t& phase, volatile int* abort_flag,
+                                         uint32_t* status) {
+  tc::mbar_arrive(bar);
+  const bool ok = tc::mbar_wait(bar, phase, abort_flag, status);
+  phase ^= 1u;
+  return ok;
+}
+
+__device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Sum N values over the 32 lanes of a warp; afterwards lane l holds the sums
+// of the heads listed by butterfly_head (N/32 of them, or 1 shared by 32/N
+// lanes when N < 32).
+template <int N>
+__device__ __forceinline__ void butterfly(float (&v)[N], int lane) {
+  int cur = N;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    if (cur >= 2) {
+      const int half = cur / 2;
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[half + i];
+          const float keep = upper ? v[half + i] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      cur = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    }
+  }
+}
+// head (within the N summed) that lane `lane` holds in slot u after butterfly<N>
+template <int N>
+__device__ __forceinline__ int butterfly_head(int lane, int u) {
+  if constexpr (N >= 32)
+    return lane * (N / 32) + u;
+  else
+    return lane / (32 / N);
+}
+
+template <int D, int DT, int H>
+__global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
+  using C_ = Cfg<D, DT, H>;
+  constexpr int STAGES = C_::STAGES, CPRS = C_::CPRS;
+  extern __shared__ __align__(1024) uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem + C_::RING_OFF;
+  uint8_t* aq = smem + C_::AQ_OFF;
+  uint8_t* ak = smem + C_::AK_OFF;
+  float* ws = reinterpret_cast<float*>(smem + C_::WS_OFF);     // [qb][0: w, 1: q_scale][H]
+  float* dws = reinterpret_cast<float*>(smem + C_::DWS_OFF);   // [4][H]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::BAR_OFF);
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = bars + STAGES;
+  uint64_t* q_full = bars + 2 * STAGES;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* x_full = q_empty + 2;
+  uint64_t* x_empty = x_full + 2;
+  uint64_t* a_full = x_empty + 2;
+  uint64_t* a_empty = a_full + 1;
+  uint64_t* dk_full = a_empty + 1;
+  uint64_t* dk_empty = dk_full + 2;
+  uint64_t* dq_full = dk_empty + 2;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* meet = dq_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C_::MISC_OFF + 4);
+  auto q_buf = [&](int qb) { return smem + C_::Q_OFF + qb * ((C_::QT + 1023) / 1024 * 1024); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ktiles = (a.k_top + 127) / 128;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      tc::mbar_init(k_full + i, kProducers);
+      tc::mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(q_full + i, kProducers);
+      tc::mbar_init(q_empty + i, 1 + 4);
+      tc::mbar_init(x_full + i, 1);
+      tc::mbar_init(x_empty + i, 4);
+      tc::mbar_init(dk_full + i, 1);
+      tc::mbar_init(dk_empty + i, 4);
+    }
+    tc::mbar_init(a_full, 128);
+    tc::mbar_init(a_empty, 1);
+    tc::mbar_init(dq_full, 1);
+    tc::mbar_init(dq_empty, 4);
+    tc::mbar_init(meet, 128);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  // the rows h' >= 2H of Aq and Ak stay zero (M = 128 > 2H)
+  for (int i = threadIdx.x; i < 2 * C_::AT / 16; i += kThreads)
+    reinterpret_cast<uint4*>(aq)[i] = make_uint4(0, 0, 0, 0);
+  tc::fence_proxy_async_smem();
+  if (warp == kTmemWarp) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const int n_mine = a.n > (int)blockIdx.x ? (a.n - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int total = n_mine * ktiles;  // tiles of this CTA
+
+  if (warp < 4) {
+    // ---------------- producers ----------------
+    const int tid = threadIdx.x;
+    constexpr int RPP = 32 / CPRS;  // rows per warp instruction
+    int stage = 0;
+    uint32_t sphase = 0;
+    for (int g = 0; g < total; ++g) {
+      const int qi = g / ktiles, i = g - qi * ktiles;
+      const int t = (int)blockIdx.x + qi * (int)gridDim.x;
+      if (i == 0) {
+        // the query's q rows (bf16, K-major = MN-major layout), w and q_scale
+        const int qb = qi & 1;
+        const bool ok = tc::mbar_wait(q_empty + qb, ((qi >> 1) & 1) ^ 1, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        uint8_t* qd = q_buf(qb);
+        constexpr int QCH = D * C_::ES / 16;  // 16-byte source chunks per q row
+        for (int f = tid; f < H * QCH; f += kProducers) {
+          const int h = f / QCH, c = f - h * QCH;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+              static_cast<const uint8_t*>(a.q) + ((size_t)t * H + h) * D * C_::ES) + c);
+          if (DT == 0) {
+            *reinterpret_cast<uint4*>(qd + sw_off(h, c * 8, H)) = v;
+          } else {
+            uint4 lo, hi;
+            e4m3x16_to_bf16(v, lo, hi);
+            *reinterpret_cast<uint4*>(qd + sw_off(h, c * 16, H)) = lo;
+            *reinterpret_cast<uint4*>(qd + sw_off(h, c * 16 + 8, H)) = hi;
+          }
+        }
+        for (int h = tid; h < H; h += kProducers) {
+          ws[(qb * 2 + 0) * H + h] = a.w[(size_t)t * H + h];
+          ws[(qb * 2 + 1) * H + h] = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(q_full + qb);
+      }
+      // this tile's 128 stored keys: lane l of warp w owns row 32w + l
+      const int j_own = i * 128 + tid;
+      int s_own = j_own < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + j_own) : -1;
+      if (s_own >= a.L) s_own = -1;
+      const bool ok = tc::mbar_wait(k_empty + stage, sphase ^ 1u, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      uint8_t* dst = ring + stage * C_::KT;
+      const int c = lane % CPRS;
+      uint4 v[CPRS];
+      int sr[CPRS];
+#pragma unroll
+      for (int p = 0; p < CPRS; ++p) {
+        const int src_lane = p * RPP + lane / CPRS;
+        sr[p] = __shfl_sync(0xffffffffu, s_own, src_lane);
+        v[p] = sr[p] >= 0 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k) +
+                                                                  (size_t)sr[p] * D * C_::ES) + c)
+                          : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int p = 0; p < CPRS; ++p) {
+        const int row = warp * 32 + p * RPP + lane / CPRS;
+        if (DT == 0) {
+          *reinterpret_cast<uint4*>(dst + sw_off(row, c * 8, 128)) = v[p];
+        } else {
+          uint4 lo, hi;
+          e4m3x16_to_bf16(v[p], lo, hi);
+          *reinterpret_cast<uint4*>(dst + sw_off(row, c * 16, 128)) = lo;
+          *reinterpret_cast<uint4*>(dst + sw_off(row, c * 16 + 8, 128)) = hi;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(k_full + stage);
+      if (++stage == STAGES) {
+        stage = 0;
+        sphase ^= 1u;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t ID_X = tc::instr_desc(0, 128, H);
+      constexpr uint32_t ID_DQ = tc::instr_desc(0, 128, D) | (1u << 15) | (1u << 16);
+      constexpr uint32_t ID_DK = tc::instr_desc(0, 128, D) | (1u << 16);
+      const uint32_t ring_a = tc::smem_u32(ring), aq_a = tc::smem_u32(aq), ak_a = tc::smem_u32(ak);
+      // forward X for tile g (keys of stage g % STAGES)
+      auto forward = [&](int g) -> bool {
+        const int qi = g / ktiles, i = g - qi * ktiles;
+        const int stage = g % STAGES;
+        if (i == 0 && !tc::mbar_wait(q_full + (qi & 1), (qi >> 1) & 1, abort_flag, a.status))
+          return false;
+        if (!tc::mbar_wait(k_full + stage, (g / STAGES) & 1, abort_flag, a.status)) return false;
+        if (!tc::mbar_wait(x_empty + (g & 1), ((g >> 1) & 1) ^ 1, abort_flag, a.status))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t qa = tc::smem_u32(q_buf(qi & 1));
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {  // K = d, 16 per step, 32 bytes
+          const uint32_t koff = (uint32_t)((j * 32) / 128), kin = (uint32_t)((j * 32) % 128);
+          const uint64_t ad = desc2(ring_a + stage * C_::KT + koff * 128 * 128 + kin, 16, 1024);
+          const uint64_t bd = desc2(qa + koff * H * 128 + kin, 16, 1024);
+          tc::mma<0>(tmem_base + C_::X_COL + (g & 1) * H, ad, bd, ID_X, j > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(x_full + (g & 1));
+        return true;
+      };
+      // dq and dk for tile g, once the epilogue has written Aq / Ak
+      auto grads = [&](int g) -> bool {
+        const int qi = g / ktiles, i = g - qi * ktiles;
+        const int stage = g % STAGES;
+        if (!tc::mbar_wait(a_full, g & 1, abort_flag, a.status)) return false;
+        if (i == 0 && !tc::mbar_wait(dq_empty, (qi & 1) ^ 1, abort_flag, a.status)) return false;
+        if (!tc::mbar_wait(dk_empty + (g & 1), ((g >> 1) & 1) ^ 1, abort_flag, a.status))
+          return false;
+        tc::fence_after_sync();
+        // DQ[h'][n] += sum_key Aq[key][h'] * Kt[key][n]: 8 steps of 16 keys
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint64_t ad = desc2(aq_a + s * 2048, 128 * 128, 1024);
+          const uint64_t bd = desc2(ring_a + stage * C_::KT + s * 2048, 128 * 128, 1024);
+          tc::mma<0>(tmem_base + C_::DQ_COL, ad, bd, ID_DQ, (i > 0 || s > 0) ? 1u : 0u);
+        }
+        // DK[key][n] = sum_h' Ak[key][h'] * Q[h' mod H][n]: high then low halves
+        const uint32_t qa = tc::smem_u32(q_buf(qi & 1));
+#pragma unroll
+        for (int s = 0; s < 2 * H / 16; ++s) {
+          const uint32_t koff = (uint32_t)((s * 32) / 128), kin = (uint32_t)((s * 32) % 128);
+          const uint64_t ad = desc2(ak_a + koff * 128 * 128 + kin, 16, 1024);
+          const uint64_t bd = desc2(qa + (s % (H / 16)) * 2048, H * 128, 1024);
+          tc::mma<0>(tmem_base + C_::DK_COL + (g & 1) * D, ad, bd, ID_DK, s > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(dk_full + (g & 1));
+        tc::mma_commit(a_empty);
+        tc::mma_commit(k_empty + stage);
+        if (i == ktiles - 1) {
+          tc::mma_commit(dq_full);
+          tc::mma_commit(q_empty + (qi & 1));
+        }
+        return true;
+      };
+      // forward of tile g + 1 goes ahead of the gradients of tile g
+      if (total > 0 && forward(0)) {
+        for (int g = 0; g < total; ++g) {
+          if (g + 1 < total && !forward(g + 1)) break;
+          if (!grads(g)) break;
+        }
+      }
+    }
+  } else if (warp >= kEpiFirstWarp) {
+    // ---------------- epilogue: TMEM lane = key ----------------
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    constexpr int NDW = H >= 32 ? H / 32 : 1;  // dw sums this lane keeps
+    float dwacc[NDW];
+    int s_prev = -1;
+    uint32_t meet_phase = 0;
+    bool ok = true;
+    for (int g = 0; g < total && ok; ++g) {
+      const int qi = g / ktiles, i = g - qi * ktiles;
+      const int t = (int)blockIdx.x + qi * (int)gridDim.x;
+      const int qb = qi & 1;
+      if (i == 0) {
+#pragma unroll
+        for (int u = 0; u < NDW; ++u) dwacc[u] = 0.0f;
+        if (!__all_sync(0xffffffffu,
+                        tc::mbar_wait(q_full + qb, (qi >> 1) & 1, abort_flag, a.status)))
+          break;
+      }
+      const float* w_s = ws + (qb * 2 + 0) * H;
+      const float* qs_s = ws + (qb * 2 + 1) * H;
+      // this row's stored key, its gradient and scale
+      const int j = i * 128 + row;
+      int s = j < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + j) : -1;
+      if (s != -1 && (s < 0 || s >= a.L)) {
+        if (a.status) atomicOr(a.status, HYTOPK_DEV_REPLAY_BAD_INDEX);
+        s = -1;
+      }
+      const float G = s >= 0 ? __ldg(a.grad + (size_t)t * a.k_top + j) : 0.0f;
+      const float ks = (s >= 0 && DT == 1) ? __ldg(a.k_scale + s) : 1.0f;
+      const float cdw = G * ks;  // dw weight of this key
+      // (a) wait for Aq / Ak to be free and X to be ready
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(a_empty, (g & 1) ^ 1, abort_flag, a.status)))
+        break;
+      if (!__all_sync(0xffffffffu,
+                      tc::mbar_wait(x_full + (g & 1), (g >> 1) & 1, abort_flag, a.status)))
+        break;
+      tc::fence_after_sync();
+      const uint32_t xaddr = tmem_base + lane_off + C_::X_COL + (g & 1) * H;
+      constexpr int CH = H < 32 ? H : 32;
+#pragma unroll
+      for (int c0 = 0; c0 < H; c0 += CH) {
+        float x[CH];
+        if (CH == 32) {
+          tc::tmem_ld32(xaddr + c0, reinterpret_cast<float(&)[32]>(x));
+          tc::tmem_wait_ld(reinterpret_cast<float(&)[32]>(x));
+        } else {
+          tc::tmem_ld16(xaddr + c0, reinterpret_cast<float(&)[16]>(x));
+          tc::tmem_wait_ld(reinterpret_cast<float(&)[16]>(x));
+        }
+        // Aq / Ak rows: 8 heads per 16-byte chunk, high parts at h', low at H + h'
+#pragma unroll
+        for (int h8 = 0; h8 < CH; h8 += 8) {
+          uint32_t qh[4], ql[4], kh[4], kl[4];
+#pragma unroll
+          for (int u = 0; u < 8; u += 2) {
+            uint16_t a0, b0, a1, b1, c0h, d0, c1, d1;
+            const int h = c0 + h8 + u;
+            const float e0 = x[h8 + u] > 0.0f ? G * w_s[h] : 0.0f;
+            const float e1 = x[h8 + u + 1] > 0.0f ? G * w_s[h + 1] : 0.0f;
+            split_bf16(e0 * ks, a0, b0);
+            split_bf16(e1 * ks, a1, b1);
+            split_bf16(e0 * qs_s[h], c0h, d0);
+            split_bf16(e1 * qs_s[h + 1], c1, d1);
+            qh[u / 2] = (uint32_t)a0 | ((uint32_t)a1 << 16);
+            ql[u / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+            kh[u / 2] = (uint32_t)c0h | ((uint32_t)c1 << 16);
+            kl[u / 2] = (uint32_t)d0 | ((uint32_t)d1 << 16);
+          }
+          const int h = c0 + h8;
+          *reinterpret_cast<uint4*>(aq + sw_off(row, h, 128)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+          *reinterpret_cast<uint4*>(aq + sw_off(row, H + h, 128)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+          *reinterpret_cast<uint4*>(ak + sw_off(row, h, 128)) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+          *reinterpret_cast<uint4*>(ak + sw_off(row, H + h, 128)) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+        }
+        // dw: sum over the warp's 32 keys of G k_scale max(0, X)
+#pragma unroll
+        for (int u = 0; u < CH; ++u) x[u] = cdw * fmaxf(x[u], 0.0f);
+        butterfly<CH>(x, lane);
+#pragma unroll
+        for (int u = 0; u < (CH >= 32 ? CH / 32 : 1); ++u) dwacc[c0 / 32 + u] += x[u];
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(x_empty + (g & 1));
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(a_full);
+      // (c) the previous tile's DK rows into dk (deferred one tile), and at the
+      // query's last tile this tile's too
+      auto drain_dk = [&](int gg, int sk) -> bool {
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(dk_full + (gg & 1), (gg >> 1) & 1, abort_flag,
+                                                   a.status)))
+          return false;
+        tc::fence_after_sync();
+        const uint32_t daddr = tmem_base + lane_off + C_::DK_COL + (gg & 1) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float v[32];
+          tc::tmem_ld32(daddr + c0, v);
+          tc::tmem_wait_ld(v);
+          if (sk >= 0) {
+            float* dst = a.dk + (size_t)sk * D + c0;
+#pragma unroll
+            for (int u = 0; u < 32; u += 4) red_add4(dst + u, v[u], v[u + 1], v[u + 2], v[u + 3]);
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(dk_empty + (gg & 1));
+        return true;
+      };
+      if (i > 0 && !drain_dk(g - 1, s_prev)) {
+        ok = false;
+        break;
+      }
+      s_prev = s;
+      if (i == ktiles - 1) {
+        if (!drain_dk(g, s)) {
+          ok = false;
+          break;
+        }
+        // DQ: rows h' < H are the high parts, H <= h' < 2H the low parts
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(dq_full, qi & 1, abort_flag, a.status))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        float* scratch = reinterpret_cast<float*>(ak);  // free: every MMA of the query is done
+        const uint32_t qaddr = tmem_base + lane_off + C_::DQ_COL;
+        // TMEM loads are warp-collective: a warp loads if any of its rows is
+        // needed, and each lane then keeps or drops its own row
+        const bool warp_has_lo = quad * 32 < 2 * H && quad * 32 + 32 > H;
+        const bool warp_has_hi = quad * 32 < H;
+        if (warp_has_lo) {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32(qaddr + c0, v);
+            tc::tmem_wait_ld(v);
+            if (row >= H && row < 2 * H) {
+#pragma unroll
+              for (int u = 0; u < 32; u += 4)
+                *reinterpret_cast<float4*>(scratch + (row - H) * D + c0 + u) =
+                    make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]);
+            }
+          }
+        }
+        // dw partials of the four warps
+#pragma unroll
+        for (int u = 0; u < NDW; ++u) {
+          if constexpr (H >= 32)
+            dws[quad * H + u * 32 + lane] = dwacc[u];
+          else if (lane % (32 / H) == 0)
+            dws[quad * H + butterfly_head<H>(lane, 0)] = dwacc[u];
+        }
+        if (!__all_sync(0xffffffffu, epi_meet(meet, meet_phase, abort_flag, a.status))) {
+          ok = false;
+          break;
+        }
+        if (warp_has_hi) {
+          float* dst = a.dq + ((size_t)t * H + (row < H ? row : 0)) * D;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32(qaddr + c0, v);
+            tc::tmem_wait_ld(v);
+            if (row < H) {
+#pragma unroll
+              for (int u = 0; u < 32; u += 4) {
+                const float4 lo = *reinterpret_cast<const float4*>(scratch + row * D + c0 + u);
+                *reinterpret_cast<float4*>(dst + c0 + u) =
+                    make_float4(v[u] + lo.x, v[u + 1] + lo.y, v[u + 2] + lo.z, v[u + 3] + lo.w);
+              }
+            }
+          }
+        }
+        if (row < H) {
+          const float dsum = (dws[row] + dws[H + row]) + (dws[2 * H + row] + dws[3 * H + row]);
+          a.dw[(size_t)t * H + row] = dsum * qs_s[row];
+        }
+        tc::fence_before_sync();
+        // scratch and dw partials read: Ak may be rewritten
+        if (!__all_sync(0xffffffffu, epi_meet(meet, meet_phase, abort_flag, a.status))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc::mbar_arrive(dq_empty);
+          tc::mbar_arrive(q_empty + qb);
+        }
+      }
+    }
+    (void)ok;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == kTmemWarp) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int D, int DT, int H>
+inline int backward_smem_bytes() {
+  return Cfg<D, DT, H>::SMEM;
+}
+
+}  // namespace bwd
+}  // namespace hytopk

@@ -176,6 +176,36 @@ hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
                             int L, int H, int d, int k_top, hytopk_dtype dt, float* scores_out,
                             uint32_t* dev_status, cudaStream_t stream);
 
+/* Gradients of the indexer score at the selected entries, with the replay
+ * rescoring fused in (Explainer, key-observation paragraph: the indexer's own
+ * loss reads only the scores at those entries; selection-replay paragraph:
+ * only those entries are rescored during recomputation). The loss is not on
+ * the pages; its gradient at the entries is the input:
+ *   grad  [n, k_top] fp32: dLoss/dI[t, idx[t,j]] (ignored where idx is -1)
+ * With qd = q * q_scale (per row of d), kd = k * k_scale and
+ * x = qd[t,h] . kd[idx[t,j]], the outputs are
+ *   dw [n, H]     fp32, written:  sum_j grad * max(0, x)
+ *   dq [n, H, d]  fp32, written:  sum_j grad * w[t,h] * [x > 0] * kd[idx[t,j]]
+ *   dk [L, d]     fp32, ADDED TO (the caller zeroes it, or accumulates over
+ *                 calls): grad * sum_h w[t,h] * [x > 0] * qd[t,h] for every
+ *                 entry, at row idx[t,j]
+ * i.e. gradients with respect to the dequantised q and k. The derivative of
+ * max(0, x) at x = 0 is 0. The tensor cores take bf16 operands: e4m3 codes
+ * convert exactly, and every product that carries a weight, gradient or
+ * scale is split into a bf16 high part and a bf16 remainder (about 16
+ * significant bits); accumulation is fp32. dk takes floating-point atomic
+ * additions, so its low bits depend on the order of arrival.
+ *   Supported: H in {16, 32, 64}, d in {64, 128}, both dtypes (others:
+ *   HYTOPK_UNSUPPORTED). dq and dk must be 16-byte aligned.
+ *   An index that is not -1 and outside [0, L) contributes nothing and sets
+ *   HYTOPK_DEV_REPLAY_BAD_INDEX in *dev_status (device uint32, may be NULL).
+ *   No workspace; asynchronous on `stream`. */
+hytopk_status hytopk_replay_backward(const void* q, const float* q_scale, const void* k,
+                                     const float* k_scale, const float* w, const int32_t* idx,
+                                     const float* grad, int n, int L, int H, int d, int k_top,
+                                     hytopk_dtype dt, float* dq, float* dk, float* dw,
+                                     uint32_t* dev_status, cudaStream_t stream);
+
 /* Bytes of workspace the two-pass path needs to hold `rows_per_chunk` rows of
  * the score table at once (rows_per_chunk <= 0: all n rows). */
 size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,

@@ -111,3 +111,23 @@ def test_sharded_host_checks(lib):
     assert call(wsb=16) == 3
     assert call(ws=P((1 << 20) + 128)) == 5
     assert call(pos=None) == 1
+
+
+def test_backward_host_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def call(**kw):
+        a = dict(q=fake, qs=None, k=fake, ks=None, w=fake, idx=fake, g=fake, n=4, L=100, H=16,
+                 d=64, k_top=8, dt=0, dq=fake, dk=fake, dw=fake, st=None)
+        a.update(kw)
+        return lib.hytopk_replay_backward(a["q"], a["qs"], a["k"], a["ks"], a["w"], a["idx"],
+                                          a["g"], a["n"], a["L"], a["H"], a["d"], a["k_top"],
+                                          a["dt"], a["dq"], a["dk"], a["dw"], a["st"], None)
+
+    assert call(H=8) == 2 and call(H=128) == 2  # H outside {16, 32, 64}
+    assert call(d=32) == 2
+    assert call(g=None) == 1 and call(idx=None) == 1 and call(dk=None) == 1
+    assert call(dt=1) == 1  # e4m3 needs scales
+    assert call(dq=P((1 << 20) + 4)) == 5
+    assert call(n=0, idx=None) == 0  # nothing to do
