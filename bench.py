@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-twopass", action="store_true")
     ap.add_argument("--no-sharded", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--shards", type=int, default=4, help="key ranges of the sharded selection")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=48, help="oracle sample size (queries)")
@@ -370,6 +371,8 @@ def gpu_arm(args, world, rank, local):
         line["twopass"] = twopass(hk, case, t, dev, idx, pairs)
     if not args.no_sharded:
         line["sharded"] = sharded(hk, case, t, dev, idx, pairs, args.shards)
+    if not args.no_backward and H in (16, 32, 64):
+        line["backward"] = backward(hk, case, t, dev, idx, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_rows)
     if rank == 0:
@@ -481,6 +484,46 @@ def sharded(hk, case, t, dev, idx_ref, pairs, P):
     del ws3
     return {"value": pairs / (ms / 1e3), "unit": "pairs/s", "ms": ms, "shards": P,
             "same_idx_as_hytopk": same}
+
+
+def backward(hk, case, t, dev, idx, pk):
+    """Gradients at the selected entries (hytopk_replay_backward) for the indices
+    of the last step and a seeded upstream gradient: 3 timed calls after one
+    warm-up, CUDA events around each call."""
+    import torch
+
+    n, H, d = case["q"].shape
+    L = case["k"].shape[0]
+    k_top = idx.shape[1]
+    es = 1 if case["dtype"] == "e4m3" else 2
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    grad = torch.randn(idx.shape, generator=gen, device=dev, dtype=torch.float32)
+    dk = torch.zeros((L, d), dtype=torch.float32, device=dev)
+    times = []
+    for rep in range(4):
+        dk.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        hk.replay_backward(t["q"], t["k"], t["w"], idx, grad, q_scale=t["q_scale"],
+                           k_scale=t["k_scale"], dk=dk)
+        b.record()
+        torch.cuda.synchronize()
+        if rep:
+            times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    entries = n * k_top
+    # DRAM bytes a perfect implementation moves: per entry idx, grad, key row and
+    # key scale; per query q, w, q_scale, dq and dw; dk read and written once
+    nbytes = (entries * (4 + 4 + d * es + (4 if es == 1 else 0)) +
+              n * (H * d * es + 4 * H * (2 if es == 1 else 1) + 4 * H * d + 4 * H) + 2 * L * d * 4)
+    flops = entries * 3 * 2 * H * d  # rescoring, dq and dk contractions
+    return {"ms": ms, "entries_per_s": entries / (ms / 1e3),
+            "algorithmic_bytes": nbytes, "achieved_gbs": nbytes / (ms / 1e3) / 1e9,
+            "frac_hbm_of_measured": nbytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+            "algorithmic_flops": flops, "achieved_tflops": flops / (ms / 1e3) / 1e12,
+            "frac_bf16_tensor_of_measured": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops"]}
 
 
 def main():

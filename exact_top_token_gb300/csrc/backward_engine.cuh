@@ -23,7 +23,8 @@
 //     DQ  [2H x d]       += Aq^T . Kt           (Aq MN-major, keys MN-major),
 //         accumulated over the query's tiles
 //     DK  [128 keys x d]  = Ak . Q              (Ak K-major, q MN-major)
-//   epilogue (warps 8-11, TMEM lane = key): from its row of X, E[h] = G w[h]
+//   epilogue (warps 8-15: two warpgroups, each for half of the heads and half
+//     of the d columns; TMEM lane = key): from its row of X, E[h] = G w[h]
 //     [X[h] > 0]; writes Aq[key][h'] = E[h] * k_scale and Ak[key][h'] =
 //     E[h] * q_scale[h], each split into a bf16 high part (h' = h) and the
 //     bf16 of the remainder (h' = H + h), so the products carry ~16 bits;
@@ -42,11 +43,13 @@
 namespace hytopk {
 namespace bwd {
 
-constexpr int kThreads = 384;
+constexpr int kGroups = 2;  // epilogue warpgroups; group g takes heads and d columns g / kGroups
+constexpr int kEpiWarps = 4 * kGroups;
 constexpr int kProducers = 128;
 constexpr int kMmaWarp = 4;
 constexpr int kTmemWarp = 5;
 constexpr int kEpiFirstWarp = 8;
+constexpr int kThreads = (kEpiFirstWarp + kEpiWarps) * 32;
 
 struct BArgs {
   const void* q;
@@ -68,7 +71,7 @@ struct Cfg {
   static constexpr int ES = DT == 0 ? 2 : 1;  // input element bytes
   static constexpr int RB = D * 2;            // bf16 row bytes in shared memory
   static constexpr int DA = RB / 128;         // 128-byte atoms per bf16 row
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = D == 128 ? 2 : 3;
   static constexpr int KT = 128 * RB;        // bf16 key tile
   static constexpr int QT = H * RB;          // bf16 q operand of one query
   static constexpr int AT = 128 * 256;       // Aq / Ak: 128 keys x 128 bf16
@@ -78,7 +81,10 @@ struct Cfg {
   static constexpr int AK_OFF = AQ_OFF + AT;
   static constexpr int WS_OFF = AK_OFF + AT;          // w, q_scale: [2][2][H] fp32
   static constexpr int DWS_OFF = WS_OFF + 2 * 2 * H * 4;  // dw partials [4][H]
-  static constexpr int BAR_OFF = DWS_OFF + 4 * H * 4;
+  // per epilogue warp: 32 rows x 32 fp32 (row stride 33) for coalescing dk additions
+  static constexpr int TR_OFF = DWS_OFF + 4 * H * 4;
+  static constexpr int TR_FLOATS = 32 * 33;
+  static constexpr int BAR_OFF = TR_OFF + kEpiWarps * TR_FLOATS * 4;
   // k_full[S], k_empty[S], q_full[2], q_empty[2], x_full[2], x_empty[2],
   // a_full, a_empty, dk_full[2], dk_empty[2], dq_full, dq_empty, epilogue meet
   static constexpr int NBARS = 2 * STAGES + 2 + 2 + 2 + 2 + 1 + 1 + 2 + 2 + 1 + 1 + 1;
@@ -233,17 +239,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(q_full + i, kProducers);
-      tc::mbar_init(q_empty + i, 1 + 4);
+      tc::mbar_init(q_empty + i, 1 + kEpiWarps);
       tc::mbar_init(x_full + i, 1);
-      tc::mbar_init(x_empty + i, 4);
+      tc::mbar_init(x_empty + i, kEpiWarps);
       tc::mbar_init(dk_full + i, 1);
-      tc::mbar_init(dk_empty + i, 4);
+      tc::mbar_init(dk_empty + i, kEpiWarps);
     }
-    tc::mbar_init(a_full, 128);
+    tc::mbar_init(a_full, 32 * kEpiWarps);
     tc::mbar_init(a_empty, 1);
     tc::mbar_init(dq_full, 1);
-    tc::mbar_init(dq_empty, 4);
-    tc::mbar_init(meet, 128);
+    tc::mbar_init(dq_empty, kEpiWarps);
+    tc::mbar_init(meet, 32 * kEpiWarps);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -407,14 +413,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
     }
   } else if (warp >= kEpiFirstWarp) {
     // ---------------- epilogue: TMEM lane = key ----------------
+    const int e = warp - kEpiFirstWarp;
+    const int gp = e / 4;                 // head / column group of this warp
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    constexpr int NDW = H >= 32 ? H / 32 : 1;  // dw sums this lane keeps
+    constexpr int HG = H / kGroups, DG = D / kGroups;
+    constexpr int CH = HG < 32 ? HG : 32;       // X columns per TMEM load
+    constexpr int NDW = HG >= 32 ? HG / 32 : 1;  // dw sums this lane keeps
+    const int h0 = gp * HG, d0 = gp * DG;
     float dwacc[NDW];
     int s_prev = -1;
     uint32_t meet_phase = 0;
     bool ok = true;
+    // this row's stored key, gradient and key scale for tile g (loaded a tile ahead)
+    auto load_entry = [&](int g, int& s, float& G, float& ks) {
+      const int qi = g / ktiles, i = g - qi * ktiles;
+      const int t = (int)blockIdx.x + qi * (int)gridDim.x;
+      const int j = i * 128 + row;
+      s = j < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + j) : -1;
+      if (s != -1 && (s < 0 || s >= a.L)) {
+        if (a.status && gp == 0) atomicOr(a.status, HYTOPK_DEV_REPLAY_BAD_INDEX);
+        s = -1;
+      }
+      G = s >= 0 ? __ldg(a.grad + (size_t)t * a.k_top + j) : 0.0f;
+      ks = (s >= 0 && DT == 1) ? __ldg(a.k_scale + s) : 1.0f;
+    };
+    int s_next = -1;
+    float G_next = 0.0f, ks_next = 1.0f;
+    if (total > 0) load_entry(0, s_next, G_next, ks_next);
     for (int g = 0; g < total && ok; ++g) {
       const int qi = g / ktiles, i = g - qi * ktiles;
       const int t = (int)blockIdx.x + qi * (int)gridDim.x;
@@ -428,15 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
       }
       const float* w_s = ws + (qb * 2 + 0) * H;
       const float* qs_s = ws + (qb * 2 + 1) * H;
-      // this row's stored key, its gradient and scale
-      const int j = i * 128 + row;
-      int s = j < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + j) : -1;
-      if (s != -1 && (s < 0 || s >= a.L)) {
-        if (a.status) atomicOr(a.status, HYTOPK_DEV_REPLAY_BAD_INDEX);
-        s = -1;
-      }
-      const float G = s >= 0 ? __ldg(a.grad + (size_t)t * a.k_top + j) : 0.0f;
-      const float ks = (s >= 0 && DT == 1) ? __ldg(a.k_scale + s) : 1.0f;
+      const int s = s_next;
+      const float G = G_next, ks = ks_next;
+      if (g + 1 < total) load_entry(g + 1, s_next, G_next, ks_next);
       const float cdw = G * ks;  // dw weight of this key
       // (a) wait for Aq / Ak to be free and X to be ready
       if (!__all_sync(0xffffffffu, tc::mbar_wait(a_empty, (g & 1) ^ 1, abort_flag, a.status)))
@@ -446,16 +467,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
         break;
       tc::fence_after_sync();
       const uint32_t xaddr = tmem_base + lane_off + C_::X_COL + (g & 1) * H;
-      constexpr int CH = H < 32 ? H : 32;
 #pragma unroll
-      for (int c0 = 0; c0 < H; c0 += CH) {
+      for (int cc = 0; cc < HG; cc += CH) {
+        const int c0 = h0 + cc;
         float x[CH];
-        if (CH == 32) {
-          tc::tmem_ld32(xaddr + c0, reinterpret_cast<float(&)[32]>(x));
-          tc::tmem_wait_ld(reinterpret_cast<float(&)[32]>(x));
+        if constexpr (CH == 32) {
+          tc::tmem_ld32(xaddr + c0, x);
+          tc::tmem_wait_ld(x);
+        } else if constexpr (CH == 16) {
+          tc::tmem_ld16(xaddr + c0, x);
+          tc::tmem_wait_ld(x);
         } else {
-          tc::tmem_ld16(xaddr + c0, reinterpret_cast<float(&)[16]>(x));
-          tc::tmem_wait_ld(reinterpret_cast<float(&)[16]>(x));
+          tc::tmem_ld8(xaddr + c0, x);
+          tc::tmem_wait_ld(x);
         }
         // Aq / Ak rows: 8 heads per 16-byte chunk, high parts at h', low at H + h'
 #pragma unroll
@@ -463,18 +487,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           uint32_t qh[4], ql[4], kh[4], kl[4];
 #pragma unroll
           for (int u = 0; u < 8; u += 2) {
-            uint16_t a0, b0, a1, b1, c0h, d0, c1, d1;
+            uint16_t a0, b0, a1, b1, c0h, d0h, c1, d1;
             const int h = c0 + h8 + u;
             const float e0 = x[h8 + u] > 0.0f ? G * w_s[h] : 0.0f;
             const float e1 = x[h8 + u + 1] > 0.0f ? G * w_s[h + 1] : 0.0f;
             split_bf16(e0 * ks, a0, b0);
             split_bf16(e1 * ks, a1, b1);
-            split_bf16(e0 * qs_s[h], c0h, d0);
+            split_bf16(e0 * qs_s[h], c0h, d0h);
             split_bf16(e1 * qs_s[h + 1], c1, d1);
             qh[u / 2] = (uint32_t)a0 | ((uint32_t)a1 << 16);
             ql[u / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
             kh[u / 2] = (uint32_t)c0h | ((uint32_t)c1 << 16);
-            kl[u / 2] = (uint32_t)d0 | ((uint32_t)d1 << 16);
+            kl[u / 2] = (uint32_t)d0h | ((uint32_t)d1 << 16);
           }
           const int h = c0 + h8;
           *reinterpret_cast<uint4*>(aq + sw_off(row, h, 128)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
@@ -486,8 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
 #pragma unroll
         for (int u = 0; u < CH; ++u) x[u] = cdw * fmaxf(x[u], 0.0f);
         butterfly<CH>(x, lane);
-#pragma unroll
-        for (int u = 0; u < (CH >= 32 ? CH / 32 : 1); ++u) dwacc[c0 / 32 + u] += x[u];
+        dwacc[cc / CH < NDW ? cc / CH : 0] += x[0];
       }
       tc::fence_before_sync();
       __syncwarp();
@@ -495,23 +518,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(a_full);
       // (c) the previous tile's DK rows into dk (deferred one tile), and at the
-      // query's last tile this tile's too
+      // query's last tile this tile's too; this group adds columns [d0, d0 + DG)
       auto drain_dk = [&](int gg, int sk) -> bool {
         if (!__all_sync(0xffffffffu, tc::mbar_wait(dk_full + (gg & 1), (gg >> 1) & 1, abort_flag,
                                                    a.status)))
           return false;
         tc::fence_after_sync();
-        const uint32_t daddr = tmem_base + lane_off + C_::DK_COL + (gg & 1) * D;
+        const uint32_t daddr = tmem_base + lane_off + C_::DK_COL + (gg & 1) * D + d0;
+        // Each lane holds its key's row; through the warp's staging block the
+        // additions go out 4 rows x 128 bytes per instruction (8 lanes per row)
+        // instead of 32 rows x 16 bytes, i.e. 4 cache lines instead of 32.
+        float* tr = reinterpret_cast<float*>(smem + C_::TR_OFF) + e * C_::TR_FLOATS;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < DG; c0 += 32) {
           float v[32];
           tc::tmem_ld32(daddr + c0, v);
           tc::tmem_wait_ld(v);
-          if (sk >= 0) {
-            float* dst = a.dk + (size_t)sk * D + c0;
 #pragma unroll
-            for (int u = 0; u < 32; u += 4) red_add4(dst + u, v[u], v[u + 1], v[u + 2], v[u + 3]);
+          for (int u = 0; u < 32; ++u) tr[lane * 33 + u] = v[u];
+          __syncwarp();
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const int r = p * 4 + lane / 8, cc = (lane % 8) * 4;
+            const int sr = __shfl_sync(0xffffffffu, sk, r);
+            if (sr >= 0) {
+              const float* src = tr + r * 33 + cc;
+              red_add4(a.dk + (size_t)sr * D + d0 + c0 + cc, src[0], src[1], src[2], src[3]);
+            }
           }
+          __syncwarp();
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -535,55 +570,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
         }
         tc::fence_after_sync();
         float* scratch = reinterpret_cast<float*>(ak);  // free: every MMA of the query is done
-        const uint32_t qaddr = tmem_base + lane_off + C_::DQ_COL;
+        const uint32_t qaddr = tmem_base + lane_off + C_::DQ_COL + d0;
         // TMEM loads are warp-collective: a warp loads if any of its rows is
         // needed, and each lane then keeps or drops its own row
         const bool warp_has_lo = quad * 32 < 2 * H && quad * 32 + 32 > H;
         const bool warp_has_hi = quad * 32 < H;
         if (warp_has_lo) {
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < DG; c0 += 32) {
             float v[32];
             tc::tmem_ld32(qaddr + c0, v);
             tc::tmem_wait_ld(v);
             if (row >= H && row < 2 * H) {
 #pragma unroll
               for (int u = 0; u < 32; u += 4)
-                *reinterpret_cast<float4*>(scratch + (row - H) * D + c0 + u) =
+                *reinterpret_cast<float4*>(scratch + (row - H) * D + d0 + c0 + u) =
                     make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]);
             }
           }
         }
-        // dw partials of the four warps
+        // dw partials of the four lane quadrants for this group's heads
 #pragma unroll
         for (int u = 0; u < NDW; ++u) {
-          if constexpr (H >= 32)
-            dws[quad * H + u * 32 + lane] = dwacc[u];
-          else if (lane % (32 / H) == 0)
-            dws[quad * H + butterfly_head<H>(lane, 0)] = dwacc[u];
+          if constexpr (CH >= 32)
+            dws[quad * H + h0 + u * 32 + lane] = dwacc[u];
+          else if (lane % (32 / CH) == 0)
+            dws[quad * H + h0 + butterfly_head<CH>(lane, 0)] = dwacc[u];
         }
         if (!__all_sync(0xffffffffu, epi_meet(meet, meet_phase, abort_flag, a.status))) {
           ok = false;
           break;
         }
         if (warp_has_hi) {
-          float* dst = a.dq + ((size_t)t * H + (row < H ? row : 0)) * D;
+          float* dst = a.dq + ((size_t)t * H + (row < H ? row : 0)) * D + d0;
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < DG; c0 += 32) {
             float v[32];
             tc::tmem_ld32(qaddr + c0, v);
             tc::tmem_wait_ld(v);
             if (row < H) {
 #pragma unroll
               for (int u = 0; u < 32; u += 4) {
-                const float4 lo = *reinterpret_cast<const float4*>(scratch + row * D + c0 + u);
+                const float4 lo =
+                    *reinterpret_cast<const float4*>(scratch + row * D + d0 + c0 + u);
                 *reinterpret_cast<float4*>(dst + c0 + u) =
                     make_float4(v[u] + lo.x, v[u + 1] + lo.y, v[u + 2] + lo.z, v[u + 3] + lo.w);
               }
             }
           }
         }
-        if (row < H) {
+        if (gp == 0 && row < H) {
           const float dsum = (dws[row] + dws[H + row]) + (dws[2 * H + row] + dws[3 * H + row]);
           a.dw[(size_t)t * H + row] = dsum * qs_s[row];
         }
