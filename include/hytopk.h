@@ -64,6 +64,14 @@
 
 #include <cuda_runtime_api.h>
 
+/* Only the functions below are exported from the shared library; every
+ * other symbol is hidden (the library is built with hidden visibility). */
+#if defined(__GNUC__)
+#define HYTOPK_API __attribute__((visibility("default")))
+#else
+#define HYTOPK_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -131,7 +139,7 @@ typedef struct {
 /* Bytes of workspace hytopk_select needs. capacity = candidate buffer slots
  * per query (0 selects the default 8 * k_top). Returns 0 for invalid or
  * unsupported arguments. */
-size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
+HYTOPK_API size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
                                     hytopk_dtype dt);
 
 /* Exact top-k selection without a score table (HyTopK).
@@ -151,14 +159,14 @@ size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k_top, int c
  * than k or more than `capacity` candidates are rescored over their whole
  * context; the candidates are radix-selected (score, then position) and
  * radix-sorted. */
-hytopk_status hytopk_select(const void* q, const float* q_scale, const void* k,
+HYTOPK_API hytopk_status hytopk_select(const void* q, const float* q_scale, const void* k,
                             const float* k_scale, const float* w, const int32_t* positions, int n,
                             int L, int H, int d, int k_top, hytopk_dtype dt, int32_t* idx_out,
                             float* scores_out, int capacity, void* workspace,
                             size_t workspace_bytes, hytopk_stats* stats_out, cudaStream_t stream);
 
 /* hytopk_select with options (opts may be NULL). */
-hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* k,
+HYTOPK_API hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* k,
                                const float* k_scale, const float* w, const int32_t* positions,
                                int n, int L, int H, int d, int k_top, hytopk_dtype dt,
                                int32_t* idx_out, float* scores_out, int capacity,
@@ -171,7 +179,7 @@ hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* 
  * idx = -1 gives -inf. Any other index outside [0, L) gives NaN and sets
  * HYTOPK_DEV_REPLAY_BAD_INDEX in *dev_status (device uint32, may be NULL).
  * Replay does not check causality. Needs no workspace. */
-hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
+HYTOPK_API hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
                             const float* k_scale, const float* w, const int32_t* idx, int n,
                             int L, int H, int d, int k_top, hytopk_dtype dt, float* scores_out,
                             uint32_t* dev_status, cudaStream_t stream);
@@ -200,7 +208,7 @@ hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
  *   An index that is not -1 and outside [0, L) contributes nothing and sets
  *   HYTOPK_DEV_REPLAY_BAD_INDEX in *dev_status (device uint32, may be NULL).
  *   No workspace; asynchronous on `stream`. */
-hytopk_status hytopk_replay_backward(const void* q, const float* q_scale, const void* k,
+HYTOPK_API hytopk_status hytopk_replay_backward(const void* q, const float* q_scale, const void* k,
                                      const float* k_scale, const float* w, const int32_t* idx,
                                      const float* grad, int n, int L, int H, int d, int k_top,
                                      hytopk_dtype dt, float* dq, float* dk, float* dw,
@@ -208,7 +216,7 @@ hytopk_status hytopk_replay_backward(const void* q, const float* q_scale, const 
 
 /* Bytes of workspace the two-pass path needs to hold `rows_per_chunk` rows of
  * the score table at once (rows_per_chunk <= 0: all n rows). */
-size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,
+HYTOPK_API size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,
                                      int rows_per_chunk);
 
 /* The conventional two-pass path (Explainer, score-table paragraph): for each
@@ -217,7 +225,7 @@ size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hyto
  * them back and selects the exact top-k with the same tie rule and order as
  * hytopk_select. The chunk size is the largest the workspace holds. Same
  * outputs as hytopk_select. */
-hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const void* k,
+HYTOPK_API hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const void* k,
                                     const float* k_scale, const float* w,
                                     const int32_t* positions, int n, int L, int H, int d,
                                     int k_top, hytopk_dtype dt, int32_t* idx_out,
@@ -247,7 +255,7 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
  * Arguments and outputs are those of hytopk_select. */
 #define HYTOPK_NOALLOC_SCRATCH_BYTES (32u << 20)
 
-hytopk_status hytopk_select_noalloc(const void* q, const float* q_scale, const void* k,
+HYTOPK_API hytopk_status hytopk_select_noalloc(const void* q, const float* q_scale, const void* k,
                                     const float* k_scale, const float* w,
                                     const int32_t* positions, int n, int L, int H, int d,
                                     int k_top, hytopk_dtype dt, int32_t* idx_out,
@@ -275,10 +283,10 @@ hytopk_status hytopk_select_noalloc(const void* q, const float* q_scale, const v
  *   ranges (a query can fail in several), fallback_used is set if any range
  *   fell back, device_status ORs the ranges' bits, n_queries = n.
  * Other arguments, outputs and errors are those of hytopk_select. */
-size_t hytopk_select_sharded_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
+HYTOPK_API size_t hytopk_select_sharded_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
                                             hytopk_dtype dt, int num_shards);
 
-hytopk_status hytopk_select_sharded(const void* q, const float* q_scale, const void* k,
+HYTOPK_API hytopk_status hytopk_select_sharded(const void* q, const float* q_scale, const void* k,
                                     const float* k_scale, const float* w,
                                     const int32_t* positions, int n, int L, int H, int d,
                                     int k_top, hytopk_dtype dt, int num_shards, int32_t* idx_out,
@@ -287,10 +295,10 @@ hytopk_status hytopk_select_sharded(const void* q, const float* q_scale, const v
                                     cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
-const char* hytopk_status_string(hytopk_status status);
+HYTOPK_API const char* hytopk_status_string(hytopk_status status);
 
 /* Library version as 10000*major + 100*minor + patch. */
-int hytopk_version(void);
+HYTOPK_API int hytopk_version(void);
 
 #ifdef __cplusplus
 }
