@@ -270,58 +270,67 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
 
   if (warp < 4) {
     // ---------------- producers ----------------
+    // Lane l of warp w owns row 32w + l of every tile (its stored key); the
+    // row copies go CPRS lanes per row, so each warp load instruction reads
+    // 32 / CPRS whole rows. When a tile's row data fits twice in registers
+    // (CPRS <= 8), the loads of tile g + 1 are issued before tile g is
+    // converted and stored, so two tiles of loads are in flight per thread.
     const int tid = threadIdx.x;
     constexpr int RPP = 32 / CPRS;  // rows per warp instruction
-    int stage = 0;
-    uint32_t sphase = 0;
-    for (int g = 0; g < total; ++g) {
+    constexpr bool kTwoInFlight = CPRS <= 8;
+    const int c = lane % CPRS;
+    auto own_key = [&](int g) -> int {
       const int qi = g / ktiles, i = g - qi * ktiles;
       const int t = (int)blockIdx.x + qi * (int)gridDim.x;
-      if (i == 0) {
-        // the query's q rows (bf16, K-major = MN-major layout), w and q_scale
-        const int qb = qi & 1;
-        const bool ok = tc::mbar_wait(q_empty + qb, ((qi >> 1) & 1) ^ 1, abort_flag, a.status);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        uint8_t* qd = q_buf(qb);
-        constexpr int QCH = D * C_::ES / 16;  // 16-byte source chunks per q row
-        for (int f = tid; f < H * QCH; f += kProducers) {
-          const int h = f / QCH, c = f - h * QCH;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              static_cast<const uint8_t*>(a.q) + ((size_t)t * H + h) * D * C_::ES) + c);
-          if (DT == 0) {
-            *reinterpret_cast<uint4*>(qd + sw_off(h, c * 8, H)) = v;
-          } else {
-            uint4 lo, hi;
-            e4m3x16_to_bf16(v, lo, hi);
-            *reinterpret_cast<uint4*>(qd + sw_off(h, c * 16, H)) = lo;
-            *reinterpret_cast<uint4*>(qd + sw_off(h, c * 16 + 8, H)) = hi;
-          }
-        }
-        for (int h = tid; h < H; h += kProducers) {
-          ws[(qb * 2 + 0) * H + h] = a.w[(size_t)t * H + h];
-          ws[(qb * 2 + 1) * H + h] = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
-        }
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(q_full + qb);
-      }
-      // this tile's 128 stored keys: lane l of warp w owns row 32w + l
-      const int j_own = i * 128 + tid;
-      int s_own = j_own < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + j_own) : -1;
-      if (s_own >= a.L) s_own = -1;
-      const bool ok = tc::mbar_wait(k_empty + stage, sphase ^ 1u, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      uint8_t* dst = ring + stage * C_::KT;
-      const int c = lane % CPRS;
-      uint4 v[CPRS];
-      int sr[CPRS];
+      const int j = i * 128 + tid;
+      int s = j < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + j) : -1;
+      return s >= a.L ? -1 : s;
+    };
+    auto issue = [&](int s_own, uint4 (&v)[CPRS]) {
 #pragma unroll
       for (int p = 0; p < CPRS; ++p) {
-        const int src_lane = p * RPP + lane / CPRS;
-        sr[p] = __shfl_sync(0xffffffffu, s_own, src_lane);
-        v[p] = sr[p] >= 0 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k) +
-                                                                  (size_t)sr[p] * D * C_::ES) + c)
-                          : make_uint4(0, 0, 0, 0);
+        const int sr = __shfl_sync(0xffffffffu, s_own, p * RPP + lane / CPRS);
+        v[p] = sr >= 0 ? __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.k) +
+                                                               (size_t)sr * D * C_::ES) + c)
+                       : make_uint4(0, 0, 0, 0);
       }
+    };
+    // the query's q rows (bf16, K-major = MN-major layout), w and q_scale
+    auto load_query = [&](int qi) -> bool {
+      const int t = (int)blockIdx.x + qi * (int)gridDim.x;
+      const int qb = qi & 1;
+      const bool ok = tc::mbar_wait(q_empty + qb, ((qi >> 1) & 1) ^ 1, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      uint8_t* qd = q_buf(qb);
+      constexpr int QCH = D * C_::ES / 16;  // 16-byte source chunks per q row
+      for (int f = tid; f < H * QCH; f += kProducers) {
+        const int h = f / QCH, cq = f - h * QCH;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+            static_cast<const uint8_t*>(a.q) + ((size_t)t * H + h) * D * C_::ES) + cq);
+        if (DT == 0) {
+          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 8, H)) = v;
+        } else {
+          uint4 lo, hi;
+          e4m3x16_to_bf16(v, lo, hi);
+          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 16, H)) = lo;
+          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 16 + 8, H)) = hi;
+        }
+      }
+      for (int h = tid; h < H; h += kProducers) {
+        ws[(qb * 2 + 0) * H + h] = a.w[(size_t)t * H + h];
+        ws[(qb * 2 + 1) * H + h] = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(q_full + qb);
+      return true;
+    };
+    // wait for tile g's stage, convert and store its rows, publish it
+    auto store = [&](int g, const uint4 (&v)[CPRS]) -> bool {
+      const int stage = g % STAGES;
+      const bool ok =
+          tc::mbar_wait(k_empty + stage, ((g / STAGES) & 1) ^ 1, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      uint8_t* dst = ring + stage * C_::KT;
 #pragma unroll
       for (int p = 0; p < CPRS; ++p) {
         const int row = warp * 32 + p * RPP + lane / CPRS;
@@ -336,9 +345,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(k_full + stage);
-      if (++stage == STAGES) {
-        stage = 0;
-        sphase ^= 1u;
+      return true;
+    };
+    if constexpr (kTwoInFlight) {
+      uint4 va[CPRS], vb[CPRS];
+      int s_next = total > 1 ? own_key(1) : -1;
+      if (total > 0) issue(own_key(0), va);
+      // tiles in pairs so that the two register buffers alternate without copies
+      for (int g = 0; g < total; g += 2) {
+        if (g % ktiles == 0 && !load_query(g / ktiles)) break;
+        if (g + 1 < total) issue(s_next, vb);
+        if (g + 2 < total) s_next = own_key(g + 2);
+        if (!store(g, va)) break;
+        if (g + 1 >= total) break;
+        if ((g + 1) % ktiles == 0 && !load_query((g + 1) / ktiles)) break;
+        if (g + 2 < total) issue(s_next, va);
+        if (g + 3 < total) s_next = own_key(g + 3);
+        if (!store(g + 1, vb)) break;
+      }
+    } else {
+      uint4 v[CPRS];
+      for (int g = 0; g < total; ++g) {
+        if (g % ktiles == 0 && !load_query(g / ktiles)) break;
+        issue(own_key(g), v);
+        if (!store(g, v)) break;
       }
     }
   } else if (warp == kMmaWarp) {
