@@ -24,13 +24,16 @@
 //         accumulated over the query's tiles
 //     DK  [128 keys x d]  = Ak . Q              (Ak K-major, q MN-major)
 //   epilogue (warps 8-15: two warpgroups, each for half of the heads and half
-//     of the d columns; TMEM lane = key): from its row of X, E[h] = G w[h]
-//     [X[h] > 0]; writes Aq[key][h'] = E[h] * k_scale and Ak[key][h'] =
-//     E[h] * q_scale[h], each split into a bf16 high part (h' = h) and the
-//     bf16 of the remainder (h' = H + h), so the products carry ~16 bits;
-//     sums G k_scale max(0, X[h]) over keys with warp butterflies (dw); adds
-//     its DK row into dk[s] with vector reductions; at the query's end adds the
-//     high and low DQ rows and writes dq[t], and writes dw[t].
+//     of the d columns; TMEM lane = key). The per-key factor c = G * k_scale
+//     and the per-head factor v[h] = w[h] * q_scale[h] are each split once
+//     into a bf16 high part and the bf16 of the remainder (~16 bits together);
+//     from its row of X the thread writes Aq[key][h'] = [X[h] > 0] * c and
+//     Ak[key][h'] = [X[h] > 0] * v[h] (high parts at h' = h, low parts at
+//     h' = H + h: a mask, no arithmetic), so DQ[h] carries no w[h] and DK[key]
+//     no G: they are applied in fp32 when DQ and DK are read out. It sums
+//     c max(0, X[h]) over keys with warp butterflies (dw), adds G * DK into
+//     dk[s] with vector reductions, and at the query's end writes
+//     dq[t, h] = w[h] (DQ[h] + DQ[H + h]) and dw[t].
 // The raw dot X uses the unscaled codes; scales are > 0, so [x > 0] =
 // [X > 0] and max(0, x) = k_scale * q_scale * max(0, X).
 #pragma once
@@ -79,8 +82,10 @@ struct Cfg {
   static constexpr int Q_OFF = RING_OFF + STAGES * KT;
   static constexpr int AQ_OFF = Q_OFF + 2 * ((QT + 1023) / 1024 * 1024);
   static constexpr int AK_OFF = AQ_OFF + AT;
-  static constexpr int WS_OFF = AK_OFF + AT;          // w, q_scale: [2][2][H] fp32
-  static constexpr int DWS_OFF = WS_OFF + 2 * 2 * H * 4;  // dw partials [4][H]
+  // per query buffer: w [H], q_scale [H] (fp32), then w * q_scale split into
+  // bf16 high / low parts packed two heads per word [H/2] + [H/2]
+  static constexpr int WS_OFF = AK_OFF + AT;
+  static constexpr int DWS_OFF = WS_OFF + 2 * 3 * H * 4;  // dw partials [4][H]
   // per epilogue warp: 32 rows x 32 fp32 (row stride 33) for coalescing dk additions
   static constexpr int TR_OFF = DWS_OFF + 4 * H * 4;
   static constexpr int TR_FLOATS = 32 * 33;
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
   uint8_t* ring = smem + C_::RING_OFF;
   uint8_t* aq = smem + C_::AQ_OFF;
   uint8_t* ak = smem + C_::AK_OFF;
-  float* ws = reinterpret_cast<float*>(smem + C_::WS_OFF);     // [qb][0: w, 1: q_scale][H]
+  float* ws = reinterpret_cast<float*>(smem + C_::WS_OFF);     // [qb][w | q_scale | pairs]
   float* dws = reinterpret_cast<float*>(smem + C_::DWS_OFF);   // [4][H]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::BAR_OFF);
   uint64_t* k_full = bars;
@@ -316,9 +321,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 16 + 8, H)) = hi;
         }
       }
+      float* wsq = ws + qb * 3 * H;
+      uint32_t* pairs = reinterpret_cast<uint32_t*>(wsq + 2 * H);
       for (int h = tid; h < H; h += kProducers) {
-        ws[(qb * 2 + 0) * H + h] = a.w[(size_t)t * H + h];
-        ws[(qb * 2 + 1) * H + h] = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+        wsq[h] = a.w[(size_t)t * H + h];
+        wsq[H + h] = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+      }
+      for (int pr = tid; pr < H / 2; pr += kProducers) {
+        const int h = 2 * pr;
+        const float s0 = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+        const float s1 = DT == 1 ? a.q_scale[(size_t)t * H + h + 1] : 1.0f;
+        uint16_t h0, l0, h1, l1;
+        split_bf16(a.w[(size_t)t * H + h] * s0, h0, l0);
+        split_bf16(a.w[(size_t)t * H + h + 1] * s1, h1, l1);
+        pairs[pr] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        pairs[H / 2 + pr] = (uint32_t)l0 | ((uint32_t)l1 << 16);
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(q_full + qb);
@@ -454,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
     const int h0 = gp * HG, d0 = gp * DG;
     float dwacc[NDW];
     int s_prev = -1;
+    float g_prev = 0.0f;
     uint32_t meet_phase = 0;
     bool ok = true;
     // this row's stored key, gradient and key scale for tile g (loaded a tile ahead)
@@ -483,12 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
                         tc::mbar_wait(q_full + qb, (qi >> 1) & 1, abort_flag, a.status)))
           break;
       }
-      const float* w_s = ws + (qb * 2 + 0) * H;
-      const float* qs_s = ws + (qb * 2 + 1) * H;
+      const float* w_s = ws + qb * 3 * H;
+      const float* qs_s = w_s + H;
+      const uint32_t* vpair = reinterpret_cast<const uint32_t*>(w_s + 2 * H);  // [hi H/2][lo H/2]
       const int s = s_next;
       const float G = G_next, ks = ks_next;
       if (g + 1 < total) load_entry(g + 1, s_next, G_next, ks_next);
-      const float cdw = G * ks;  // dw weight of this key
+      const float cdw = G * ks;  // the key's factor c (and its dw weight)
+      uint32_t chh, cll;  // c split into bf16 high / low parts, repeated in both halves
+      {
+        uint16_t ch, cl;
+        split_bf16(cdw, ch, cl);
+        chh = (uint32_t)ch * 0x10001u;
+        cll = (uint32_t)cl * 0x10001u;
+      }
       // (a) wait for Aq / Ak to be free and X to be ready
       if (!__all_sync(0xffffffffu, tc::mbar_wait(a_empty, (g & 1) ^ 1, abort_flag, a.status)))
         break;
@@ -515,20 +541,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
 #pragma unroll
         for (int h8 = 0; h8 < CH; h8 += 8) {
           uint32_t qh[4], ql[4], kh[4], kl[4];
+          const uint4 vh = *reinterpret_cast<const uint4*>(vpair + (c0 + h8) / 2);
+          const uint4 vl = *reinterpret_cast<const uint4*>(vpair + H / 2 + (c0 + h8) / 2);
+          const uint32_t vhs[4] = {vh.x, vh.y, vh.z, vh.w}, vls[4] = {vl.x, vl.y, vl.z, vl.w};
 #pragma unroll
           for (int u = 0; u < 8; u += 2) {
-            uint16_t a0, b0, a1, b1, c0h, d0h, c1, d1;
-            const int h = c0 + h8 + u;
-            const float e0 = x[h8 + u] > 0.0f ? G * w_s[h] : 0.0f;
-            const float e1 = x[h8 + u + 1] > 0.0f ? G * w_s[h + 1] : 0.0f;
-            split_bf16(e0 * ks, a0, b0);
-            split_bf16(e1 * ks, a1, b1);
-            split_bf16(e0 * qs_s[h], c0h, d0h);
-            split_bf16(e1 * qs_s[h + 1], c1, d1);
-            qh[u / 2] = (uint32_t)a0 | ((uint32_t)a1 << 16);
-            ql[u / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
-            kh[u / 2] = (uint32_t)c0h | ((uint32_t)c1 << 16);
-            kl[u / 2] = (uint32_t)d0h | ((uint32_t)d1 << 16);
+            // [X > 0] of the two heads as a mask over their 16-bit halves
+            const uint32_t m = (x[h8 + u] > 0.0f ? 0x0000FFFFu : 0u) |
+                               (x[h8 + u + 1] > 0.0f ? 0xFFFF0000u : 0u);
+            qh[u / 2] = chh & m;
+            ql[u / 2] = cll & m;
+            kh[u / 2] = vhs[u / 2] & m;
+            kl[u / 2] = vls[u / 2] & m;
           }
           const int h = c0 + h8;
           *reinterpret_cast<uint4*>(aq + sw_off(row, h, 128)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
@@ -549,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
       tc::mbar_arrive(a_full);
       // (c) the previous tile's DK rows into dk (deferred one tile), and at the
       // query's last tile this tile's too; this group adds columns [d0, d0 + DG)
-      auto drain_dk = [&](int gg, int sk) -> bool {
+      auto drain_dk = [&](int gg, int sk, float gk) -> bool {
         if (!__all_sync(0xffffffffu, tc::mbar_wait(dk_full + (gg & 1), (gg >> 1) & 1, abort_flag,
                                                    a.status)))
           return false;
@@ -565,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           tc::tmem_ld32(daddr + c0, v);
           tc::tmem_wait_ld(v);
 #pragma unroll
-          for (int u = 0; u < 32; ++u) tr[lane * 33 + u] = v[u];
+          for (int u = 0; u < 32; ++u) tr[lane * 33 + u] = gk * v[u];
           __syncwarp();
 #pragma unroll
           for (int p = 0; p < 8; ++p) {
@@ -583,13 +607,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
         if (lane == 0) tc::mbar_arrive(dk_empty + (gg & 1));
         return true;
       };
-      if (i > 0 && !drain_dk(g - 1, s_prev)) {
+      if (i > 0 && !drain_dk(g - 1, s_prev, g_prev)) {
         ok = false;
         break;
       }
       s_prev = s;
+      g_prev = G;
       if (i == ktiles - 1) {
-        if (!drain_dk(g, s)) {
+        if (!drain_dk(g, s, G)) {
           ok = false;
           break;
         }
@@ -639,12 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
             tc::tmem_ld32(qaddr + c0, v);
             tc::tmem_wait_ld(v);
             if (row < H) {
+              const float wh = w_s[row];
 #pragma unroll
               for (int u = 0; u < 32; u += 4) {
                 const float4 lo =
                     *reinterpret_cast<const float4*>(scratch + row * D + d0 + c0 + u);
                 *reinterpret_cast<float4*>(dst + c0 + u) =
-                    make_float4(v[u] + lo.x, v[u + 1] + lo.y, v[u + 2] + lo.z, v[u + 3] + lo.w);
+                    make_float4(wh * (v[u] + lo.x), wh * (v[u + 1] + lo.y),
+                                wh * (v[u + 2] + lo.z), wh * (v[u + 3] + lo.w));
               }
             }
           }
