@@ -58,7 +58,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
         return r.stderr
 
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+    with cf.ThreadPoolExecutor(max_workers=min(16, len(srcs))) as ex:
         logs = list(ex.map(compile_one, zip(srcs, objs)))
     if verbose:
         for s, log in zip(srcs, logs):

@@ -15,7 +15,10 @@ constexpr int kVersion = 100;  // 0.1.0
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool supported_h(int H) { return H >= 1 && H <= 128 && (H & (H - 1)) == 0; }
-bool supported_d(int d) { return d == 64 || d == 128; }
+// rows of 64, 128 or 256 bytes: bf16 d = 32, 64, 128; e4m3 d = 64, 128, 256
+bool supported_d(int d, hytopk_dtype dt) {
+  return dt == HYTOPK_BF16 ? (d == 32 || d == 64 || d == 128) : (d == 64 || d == 128 || d == 256);
+}
 int elem_size(hytopk_dtype dt) { return dt == HYTOPK_BF16 ? 2 : 1; }
 bool valid_dtype(hytopk_dtype dt) { return dt == HYTOPK_BF16 || dt == HYTOPK_E4M3; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -92,7 +95,7 @@ namespace hytopk {
 // Shape checks shared by every entry point.
 hytopk_status check_shape(int n, int L, int H, int d, int k_top, hytopk_dtype dt) {
   if (n < 0 || L < 1 || H < 1 || d < 1 || k_top < 1 || !valid_dtype(dt)) return HYTOPK_INVALID_ARG;
-  if (!supported_h(H) || !supported_d(d) || k_top > kMaxTopK) return HYTOPK_UNSUPPORTED;
+  if (!supported_h(H) || !supported_d(d, dt) || k_top > kMaxTopK) return HYTOPK_UNSUPPORTED;
   if (n > (1 << 22) || L > (1 << 30)) return HYTOPK_UNSUPPORTED;
   return HYTOPK_OK;
 }

@@ -21,7 +21,7 @@ extern "C" hytopk_status hytopk_replay_backward(const void* q, const float* q_sc
   hytopk_status s = check_shape(n, L, H, d, k_top, dt);
   if (s != HYTOPK_OK) return s;
   if ((s = check_inputs(q, q_scale, k, k_scale, w, dt, n)) != HYTOPK_OK) return s;
-  if (H != 16 && H != 32 && H != 64) return HYTOPK_UNSUPPORTED;
+  if ((H != 16 && H != 32 && H != 64) || (d != 64 && d != 128)) return HYTOPK_UNSUPPORTED;
   if (n == 0) return HYTOPK_OK;
   if (!idx || !grad || !dq || !dk || !dw) return HYTOPK_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dq) & 15u) || (reinterpret_cast<uintptr_t>(dk) & 15u))

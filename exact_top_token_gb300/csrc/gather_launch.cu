@@ -13,17 +13,24 @@ cudaError_t launch_gather_d128_bf16(int H, int mode, const gather::GArgs& a, int
                                     cudaStream_t st);
 cudaError_t launch_gather_d128_e4m3(int H, int mode, const gather::GArgs& a, int grid,
                                     cudaStream_t st);
+cudaError_t launch_gather_d32_bf16(int H, int mode, const gather::GArgs& a, int grid,
+                                   cudaStream_t st);
+cudaError_t launch_gather_d256_e4m3(int H, int mode, const gather::GArgs& a, int grid,
+                                    cudaStream_t st);
 
 namespace {
 
 cudaError_t dispatch(const Problem& p, int mode, const gather::GArgs& a, int grid,
                      cudaStream_t st) {
   if (grid <= 0) return cudaSuccess;
-  if (p.d == 64)
-    return p.dt == 0 ? launch_gather_d64_bf16(p.H, mode, a, grid, st)
-                     : launch_gather_d64_e4m3(p.H, mode, a, grid, st);
-  return p.dt == 0 ? launch_gather_d128_bf16(p.H, mode, a, grid, st)
-                   : launch_gather_d128_e4m3(p.H, mode, a, grid, st);
+  if (p.dt == 0) {
+    if (p.d == 32) return launch_gather_d32_bf16(p.H, mode, a, grid, st);
+    if (p.d == 64) return launch_gather_d64_bf16(p.H, mode, a, grid, st);
+    return launch_gather_d128_bf16(p.H, mode, a, grid, st);
+  }
+  if (p.d == 64) return launch_gather_d64_e4m3(p.H, mode, a, grid, st);
+  if (p.d == 128) return launch_gather_d128_e4m3(p.H, mode, a, grid, st);
+  return launch_gather_d256_e4m3(p.H, mode, a, grid, st);
 }
 
 gather::GArgs base_args(const Problem& p) {

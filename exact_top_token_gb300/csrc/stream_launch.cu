@@ -14,6 +14,10 @@ cudaError_t launch_stream_d128_bf16(int H, int mode, const CUtensorMap& km, cons
                                     const stream::Args& a, int grid, cudaStream_t st);
 cudaError_t launch_stream_d128_e4m3(int H, int mode, const CUtensorMap& km, const CUtensorMap& qm,
                                     const stream::Args& a, int grid, cudaStream_t st);
+cudaError_t launch_stream_d32_bf16(int H, int mode, const CUtensorMap& km, const CUtensorMap& qm,
+                                   const stream::Args& a, int grid, cudaStream_t st);
+cudaError_t launch_stream_d256_e4m3(int H, int mode, const CUtensorMap& km, const CUtensorMap& qm,
+                                    const stream::Args& a, int grid, cudaStream_t st);
 
 namespace {
 
@@ -22,11 +26,14 @@ int atom_bytes(const Problem& p) { return row_bytes(p) >= 128 ? 128 : 64; }
 
 cudaError_t dispatch(const Problem& p, int mode, const CUtensorMap& km, const CUtensorMap& qm,
                      const stream::Args& a, int grid, cudaStream_t st) {
-  if (p.d == 64)
-    return p.dt == 0 ? launch_stream_d64_bf16(p.H, mode, km, qm, a, grid, st)
-                     : launch_stream_d64_e4m3(p.H, mode, km, qm, a, grid, st);
-  return p.dt == 0 ? launch_stream_d128_bf16(p.H, mode, km, qm, a, grid, st)
-                   : launch_stream_d128_e4m3(p.H, mode, km, qm, a, grid, st);
+  if (p.dt == 0) {
+    if (p.d == 32) return launch_stream_d32_bf16(p.H, mode, km, qm, a, grid, st);
+    if (p.d == 64) return launch_stream_d64_bf16(p.H, mode, km, qm, a, grid, st);
+    return launch_stream_d128_bf16(p.H, mode, km, qm, a, grid, st);
+  }
+  if (p.d == 64) return launch_stream_d64_e4m3(p.H, mode, km, qm, a, grid, st);
+  if (p.d == 128) return launch_stream_d128_e4m3(p.H, mode, km, qm, a, grid, st);
+  return launch_stream_d256_e4m3(p.H, mode, km, qm, a, grid, st);
 }
 
 bool key_map(const Problem& p, CUtensorMap* km) {

@@ -49,9 +49,11 @@
  *     must be finite and > 0 (then ReLU(a*x) = a*ReLU(x) and scales may be
  *     applied after the dot); a non-positive scale sets HYTOPK_DEV_BAD_SCALE.
  *     Inputs must be finite.
- *   - Supported shapes: H in {1,2,4,8,16,32,64,128}, d in {64,128}, d*elem
- *     size a multiple of 16 bytes; 1 <= k_top <= 16384; n >= 0; L >= 1.
- *     Other shapes return HYTOPK_UNSUPPORTED.
+ *   - Supported shapes: H in {1,2,4,8,16,32,64,128}; key rows of 64, 128 or
+ *     256 bytes, i.e. d in {32, 64, 128} for bf16 and d in {64, 128, 256} for
+ *     e4m3; 1 <= k_top <= 16384; n >= 0; L >= 1 (hytopk_replay_backward:
+ *     H in {16, 32, 64}, d in {64, 128}). Other shapes return
+ *     HYTOPK_UNSUPPORTED.
  *   - Device pointers must be 16-byte aligned.
  *   - Scores are fp32. A selected score agrees with the definition above to
  *     within 1e-3 relative (exact for integer-valued data that fits fp32).

@@ -39,6 +39,15 @@ def test_status_strings_and_version(lib):
     assert lib.hytopk_version() >= 100
 
 
+def test_supported_row_shapes(lib):
+    """Rows of 64, 128 or 256 bytes: bf16 d = 32, 64, 128; e4m3 d = 64, 128, 256."""
+    ws = lib.hytopk_select_workspace_size
+    for d, dt, ok in [(32, 0, True), (64, 0, True), (128, 0, True), (256, 0, False),
+                      (32, 1, False), (64, 1, True), (128, 1, True), (256, 1, True),
+                      (96, 0, False), (16, 0, False)]:
+        assert (ws(64, 4096, 4, d, 256, 0, dt) > 0) == ok, (d, dt)
+
+
 def test_workspace_size_rules(lib):
     ws = lib.hytopk_select_workspace_size
     assert ws(64, 4096, 4, 64, 256, 0, 0) > 0
@@ -68,7 +77,8 @@ def test_host_checks_reject_bad_arguments(lib):
     assert call(k=None) == 1
     assert call(n=-1) == 1
     assert call(H=6) == 2
-    assert call(d=32) == 2
+    assert call(d=48) == 2
+    assert call(d=256) == 2  # bf16 rows of 512 bytes
     assert call(k_top=20000) == 2
     assert call(dt=1) == 1  # e4m3 needs scales
     assert call(qs=fake) == 1  # bf16 takes no scales

@@ -85,6 +85,9 @@ def test_recovery_stress_full_fallback(hk, dev):
     (700, 5, 128, 128, 64, "bf16", "random"),
     (4500, 40, 8, 64, 1, "bf16", "random"),
     (130, 7, 2, 128, 200, "e4m3", "random"),
+    (4000, 50, 16, 32, 256, "bf16", "random"),     # 64-byte bf16 rows
+    (6000, 40, 64, 256, 300, "e4m3", "random"),    # 256-byte e4m3 rows
+    (300, 9, 8, 256, 500, "e4m3", "last"),         # ctx < k
 ])
 def test_random_small(hk, dev, L, n, H, d, k_top, dt, pos):
     case = si.random_case(L, n, H, d, k_top, dt, seed=L + n, positions=pos)
@@ -228,14 +231,16 @@ def test_replay_parity_and_bad_indices(hk, dev):
     assert int(status.item()) & hk.DEV_REPLAY_BAD_INDEX
 
 
-def test_replay_random_indices_vs_oracle(hk, dev):
+@pytest.mark.parametrize("d,dt", [(64, "bf16"), (32, "bf16"), (256, "e4m3")])
+def test_replay_random_indices_vs_oracle(hk, dev, d, dt):
     import torch
 
-    case = si.random_case(4000, 37, 16, 64, 333, "bf16", seed=25, positions="last")
+    case = si.random_case(4000, 37, 16, d, 333, dt, seed=25, positions="last")
     g = np.random.Generator(np.random.PCG64(26))
     idx = g.integers(-1, 4000, size=(37, 333)).astype(np.int32)
     t = si.to_torch(case, dev)
-    rs = hk.replay(t["q"], t["k"], t["w"], torch.from_numpy(idx).to(dev))
+    rs = hk.replay(t["q"], t["k"], t["w"], torch.from_numpy(idx).to(dev), q_scale=t["q_scale"],
+                   k_scale=t["k_scale"])
     ref, bad = oracle.replay(case, idx)
     got = rs.cpu().numpy()
     assert bad == 0
@@ -260,6 +265,31 @@ def test_twopass_matches_select(hk, dev, chunk):
     i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], 400, workspace=ws)
     assert np.array_equal(i2.cpu().numpy(), idx.cpu().numpy())
     assert np.array_equal(s2.cpu().numpy(), sc.cpu().numpy())
+
+
+@pytest.mark.parametrize("d,dt", [(32, "bf16"), (256, "e4m3")])
+def test_new_row_shapes_exact_and_consistent(hk, dev, d, dt):
+    """Integer data with the new row shapes: exact against the oracle, and the
+    two-pass path and replay agree with the selection bit for bit."""
+    case = si.random_case(3000, 30, 8, d, 200, "bf16", seed=d, positions="spaced", kind="int")
+    if dt == "e4m3":
+        import torch
+
+        qf = si.bf16_bits_to_f32(case["q"])
+        kf = si.bf16_bits_to_f32(case["k"])
+        case = dict(case, dtype="e4m3",
+                    q=torch.from_numpy(qf).to(torch.float8_e4m3fn).view(torch.uint8).numpy(),
+                    k=torch.from_numpy(kf).to(torch.float8_e4m3fn).view(torch.uint8).numpy(),
+                    q_scale=np.ones(qf.shape[:2], np.float32),
+                    k_scale=np.ones(kf.shape[0], np.float32))
+    idx, sc, _, t = run_select(hk, case, dev)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(30), gi, gs, exact=True)
+    i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], case["k_top"],
+                               q_scale=t["q_scale"], k_scale=t["k_scale"])
+    assert np.array_equal(i2.cpu().numpy(), gi) and np.array_equal(s2.cpu().numpy(), gs)
+    rs = hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"])
+    assert np.array_equal(rs.cpu().numpy(), gs)
 
 
 def test_twopass_exact_on_integer_data(hk, dev):
