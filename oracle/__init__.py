@@ -32,7 +32,7 @@ _SO = os.path.join(_BUILD, "libhytopk_oracle.so")
 
 CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared"]
 
-_DTYPES = {"bf16": 0, "e4m3": 1}
+_DTYPES = {"bf16": 0, "e4m3": 1, "e4m3_bf16": 2}
 _lib = None
 
 

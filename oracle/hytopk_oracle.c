@@ -31,7 +31,8 @@
  *   Inputs: bf16 (bit shift to fp32) or OCP FP8 E4M3 ("fn": bias 7, no
  *     infinities, S.1111.111 is NaN, max 448) times an fp32 scale per
  *     128-element row: q_scale[t,h], k_scale[s]. The scale is applied to the
- *     element before the dot.
+ *     element before the dot. dtype 2 is e4m3 q (with q_scale) and bf16 k
+ *     (without a scale).
  *   -0.0 scores are canonicalised to +0.0.
  *   Exact top-k (Explainer, HyTopK paragraph): order all (I, s), s < ctx, by
  *     I descending, then s ascending (READING: the lower position wins a tie
@@ -68,6 +69,11 @@
 
 #define ORACLE_BF16 0
 #define ORACLE_E4M3 1
+#define ORACLE_E4M3_BF16 2 /* q e4m3 with q_scale, k bf16 without a scale */
+
+static int q_dtype(int dtype) { return dtype == ORACLE_BF16 ? ORACLE_BF16 : ORACLE_E4M3; }
+static int k_dtype(int dtype) { return dtype == ORACLE_E4M3 ? ORACLE_E4M3 : ORACLE_BF16; }
+static int valid_dtype(int dtype) { return dtype >= ORACLE_BF16 && dtype <= ORACLE_E4M3_BF16; }
 
 #define ORACLE_OK 0
 #define ORACLE_BAD_ARG 1
@@ -152,16 +158,18 @@ static float element(const void* base, int dtype, size_t i) {
 static int setup(problem* p) {
   size_t L = (size_t)p->L, d = (size_t)p->d;
   if (p->L <= 0 || p->H <= 0 || p->d <= 0 || p->n < 0) return ORACLE_BAD_ARG;
-  if (p->dtype != ORACLE_BF16 && p->dtype != ORACLE_E4M3) return ORACLE_BAD_ARG;
-  if (p->dtype == ORACLE_E4M3 && (!p->q_scale || !p->k_scale)) return ORACLE_BAD_ARG;
+  if (!valid_dtype(p->dtype)) return ORACLE_BAD_ARG;
+  if (q_dtype(p->dtype) == ORACLE_E4M3 && !p->q_scale) return ORACLE_BAD_ARG;
+  if (k_dtype(p->dtype) == ORACLE_E4M3 && !p->k_scale) return ORACLE_BAD_ARG;
   p->kf = (float*)malloc(L * d * sizeof(float));
   if (!p->kf) return ORACLE_NO_MEMORY;
 #pragma omp parallel for schedule(static)
   for (int64_t s = 0; s < p->L; ++s) {
-    float scale = p->dtype == ORACLE_E4M3 ? p->k_scale[s] : 1.0f;
+    const int kd = k_dtype(p->dtype);
+    float scale = kd == ORACLE_E4M3 ? p->k_scale[s] : 1.0f;
     for (size_t i = 0; i < d; ++i) {
-      float v = element(p->k, p->dtype, (size_t)s * d + i);
-      p->kf[(size_t)s * d + i] = p->dtype == ORACLE_E4M3 ? v * scale : v;
+      float v = element(p->k, kd, (size_t)s * d + i);
+      p->kf[(size_t)s * d + i] = kd == ORACLE_E4M3 ? v * scale : v;
     }
   }
   return ORACLE_OK;
@@ -172,11 +180,12 @@ static int setup(problem* p) {
  * order). */
 static void query_operand(const problem* p, int64_t t, float* qT) {
   for (int h = 0; h < p->H; ++h) {
-    float scale = p->dtype == ORACLE_E4M3 ? p->q_scale[t * p->H + h] : 1.0f;
+    const int qd = q_dtype(p->dtype);
+    float scale = qd == ORACLE_E4M3 ? p->q_scale[t * p->H + h] : 1.0f;
     for (int i = 0; i < p->d; ++i) {
       size_t at = ((size_t)t * p->H + h) * p->d + i;
-      float v = element(p->q, p->dtype, at);
-      qT[(size_t)i * p->H + h] = p->dtype == ORACLE_E4M3 ? v * scale : v;
+      float v = element(p->q, qd, at);
+      qT[(size_t)i * p->H + h] = qd == ORACLE_E4M3 ? v * scale : v;
     }
   }
 }
@@ -425,8 +434,9 @@ int oracle_backward(const void* q, const float* q_scale, const void* k, const fl
                     double* dw, double* dq_abs, double* dk_abs, double* dw_abs, double* dq_amb,
                     double* dk_amb, double* dw_amb, int64_t* bad, int nthreads) {
   if (n < 0 || L <= 0 || H <= 0 || d <= 0 || k_top <= 0) return ORACLE_BAD_ARG;
-  if (dtype != ORACLE_BF16 && dtype != ORACLE_E4M3) return ORACLE_BAD_ARG;
-  if (dtype == ORACLE_E4M3 && (!q_scale || !k_scale)) return ORACLE_BAD_ARG;
+  if (!valid_dtype(dtype)) return ORACLE_BAD_ARG;
+  if (q_dtype(dtype) == ORACLE_E4M3 && !q_scale) return ORACLE_BAD_ARG;
+  if (k_dtype(dtype) == ORACLE_E4M3 && !k_scale) return ORACLE_BAD_ARG;
   const size_t Hd = (size_t)H * d;
   /* dequantised keys and their norms, fp64 (the products are exact) */
   double* kd = (double*)malloc((size_t)L * d * sizeof(double));
@@ -439,10 +449,10 @@ int oracle_backward(const void* q, const float* q_scale, const void* k, const fl
   set_threads(nthreads);
 #pragma omp parallel for schedule(static)
   for (int64_t s = 0; s < L; ++s) {
-    double scale = dtype == ORACLE_E4M3 ? (double)k_scale[s] : 1.0;
+    double scale = k_dtype(dtype) == ORACLE_E4M3 ? (double)k_scale[s] : 1.0;
     double nn = 0.0;
     for (int i = 0; i < d; ++i) {
-      double v = (double)element(k, dtype, (size_t)s * d + i) * scale;
+      double v = (double)element(k, k_dtype(dtype), (size_t)s * d + i) * scale;
       kd[(size_t)s * d + i] = v;
       nn += v * v;
     }
@@ -462,10 +472,10 @@ int oracle_backward(const void* q, const float* q_scale, const void* k, const fl
 #pragma omp for schedule(dynamic, 4)
     for (int64_t t = 0; t < n; ++t) {
       for (int h = 0; h < H; ++h) {
-        double scale = dtype == ORACLE_E4M3 ? (double)q_scale[t * H + h] : 1.0;
+        double scale = q_dtype(dtype) == ORACLE_E4M3 ? (double)q_scale[t * H + h] : 1.0;
         double nn = 0.0;
         for (int i = 0; i < d; ++i) {
-          double v = (double)element(q, dtype, ((size_t)t * H + h) * d + i) * scale;
+          double v = (double)element(q, q_dtype(dtype), ((size_t)t * H + h) * d + i) * scale;
           qd[(size_t)h * d + i] = v;
           nn += v * v;
         }
@@ -515,10 +525,10 @@ int oracle_backward(const void* q, const float* q_scale, const void* k, const fl
   double* qnorm = (double*)malloc((size_t)H * sizeof(double));
   for (int64_t t = 0; t < n && qd && qnorm; ++t) {
     for (int h = 0; h < H; ++h) {
-      double scale = dtype == ORACLE_E4M3 ? (double)q_scale[t * H + h] : 1.0;
+      double scale = q_dtype(dtype) == ORACLE_E4M3 ? (double)q_scale[t * H + h] : 1.0;
       double nn = 0.0;
       for (int i = 0; i < d; ++i) {
-        double v = (double)element(q, dtype, ((size_t)t * H + h) * d + i) * scale;
+        double v = (double)element(q, q_dtype(dtype), ((size_t)t * H + h) * d + i) * scale;
         qd[(size_t)h * d + i] = v;
         nn += v * v;
       }

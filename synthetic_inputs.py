@@ -60,6 +60,14 @@ def e4m3_encode_rows(x):
     return codes, scale
 
 
+def element_types(dtype):
+    """(q element type, k element type) of a case dtype: "bf16", "e4m3", or
+    "e4m3_bf16" (e4m3 q with a per-row scale, bf16 k without one)."""
+    if dtype == "e4m3_bf16":
+        return "e4m3", "bf16"
+    return dtype, dtype
+
+
 def _encode(x, dtype):
     if dtype == "bf16":
         return f32_to_bf16_bits(x), None
@@ -105,8 +113,9 @@ def random_case(L, n, H, d, k_top, dtype="bf16", seed=0, positions="last", kind=
             raise ValueError(positions)
     else:
         pos = np.ascontiguousarray(positions, dtype=np.int32)
-    q, q_scale = _encode(qf, dtype)
-    k, k_scale = _encode(kf, dtype)
+    qdt, kdt = element_types(dtype)
+    q, q_scale = _encode(qf, qdt)
+    k, k_scale = _encode(kf, kdt)
     return {"q": q, "q_scale": q_scale, "k": k, "k_scale": k_scale, "w": w.astype(np.float32),
             "positions": pos, "dtype": dtype, "k_top": int(k_top),
             "name": name or f"random_{kind}_{dtype}_L{L}_n{n}_H{H}_d{d}_k{k_top}"}
@@ -243,11 +252,10 @@ def to_torch(case, device="cuda"):
     def t(a):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
-    if case["dtype"] == "bf16":
-        q = t(case["q"].view(np.int16)).view(torch.bfloat16)
-        k = t(case["k"].view(np.int16)).view(torch.bfloat16)
-    else:
-        q = t(case["q"]).view(torch.float8_e4m3fn)
-        k = t(case["k"]).view(torch.float8_e4m3fn)
+    qdt, kdt = element_types(case["dtype"])
+    q = (t(case["q"].view(np.int16)).view(torch.bfloat16) if qdt == "bf16"
+         else t(case["q"]).view(torch.float8_e4m3fn))
+    k = (t(case["k"].view(np.int16)).view(torch.bfloat16) if kdt == "bf16"
+         else t(case["k"]).view(torch.float8_e4m3fn))
     return {"q": q, "k": k, "q_scale": t(case["q_scale"]), "k_scale": t(case["k_scale"]),
             "w": t(case["w"]), "positions": t(case["positions"]), "k_top": case["k_top"]}

@@ -35,6 +35,8 @@ MUTANTS = [
     ("sample_midpoint", "return (j * ctx) / m;", "return (j * ctx + ctx / 2) / m;"),
     ("subnormal_exp", "v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
     ("e4m3_bias", "v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("mixed_q_as_bf16", "static int q_dtype(int dtype) { return dtype == ORACLE_BF16 ? ORACLE_BF16 : ORACLE_E4M3; }",
+     "static int q_dtype(int dtype) { return dtype == ORACLE_E4M3 ? ORACLE_E4M3 : ORACLE_BF16; }"),
     # the backward at selected entries
     ("bwd_dq_no_weight", "dqt[e] += coef * ks[i];", "dqt[e] += g * ks[i];"),
     ("bwd_dk_uses_key", "dk[e] += coef * qd[(size_t)h * d + i];", "dk[e] += coef * ks[i];"),
@@ -65,6 +67,7 @@ def battery():
         pins.test_filter_full_sampling_threshold_is_exact_rank,
         pins.test_filter_certificate_holds,
         pins.test_filter_threshold_rank_on_distinct_scores,
+        pins.test_mixed_e4m3_q_bf16_k_reduces_to_bf16,
         bpins.test_dw_is_the_difference_in_w,
         bpins.test_dq_is_the_difference_in_q,
         bpins.test_dk_is_the_difference_in_k,

@@ -351,3 +351,34 @@ def test_replay_equals_selected_scores_and_flags_bad_indices():
     idx2[1, 1] = -5
     rs2, bad2 = oracle.replay(case, idx2)
     assert bad2 == 2 and math.isnan(rs2[0, 0]) and math.isnan(rs2[1, 1])
+
+
+def test_mixed_e4m3_q_bf16_k_reduces_to_bf16():
+    """e4m3 q (power-of-two q_scale) with bf16 k equals the bf16 problem whose q
+    is those values, exactly (every such value is a bf16 value): selection,
+    replay and backward."""
+    import torch
+
+    g = si.rng_for(31)
+    n, H, d, L, k_top = 6, 4, 16, 300, 20
+    codes = g.choice([0x38, 0x40, 0xB8, 0x44, 0xC0, 0x30, 0x00], size=(n, H, d)).astype(np.uint8)
+    qs = np.exp2(g.integers(-2, 3, size=(n, H))).astype(np.float32)
+    qf = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy() * qs[:, :, None]
+    kf = g.integers(-3, 4, size=(L, d)).astype(np.float32)
+    base = {"k": si.f32_to_bf16_bits(kf), "k_scale": None,
+            "w": g.integers(1, 3, size=(n, H)).astype(np.float32),
+            "positions": np.array([299, 250, 120, 40, 10, 299], np.int32), "k_top": k_top,
+            "name": "mixed"}
+    mixed = dict(base, q=codes, q_scale=qs, dtype="e4m3_bf16")
+    plain = dict(base, q=si.f32_to_bf16_bits(qf), q_scale=None, dtype="bf16")
+    i1, s1 = oracle.select(mixed)
+    i2, s2 = oracle.select(plain)
+    assert np.array_equal(i1, i2) and np.array_equal(s1, s2)
+    idx = i1.copy()
+    r1, _ = oracle.replay(mixed, idx)
+    r2, _ = oracle.replay(plain, idx)
+    assert np.array_equal(r1, r2)
+    grad = g.integers(-2, 3, size=idx.shape).astype(np.float32)
+    b1, b2 = oracle.backward(mixed, idx, grad), oracle.backward(plain, idx, grad)
+    for key in ("dq", "dk", "dw"):
+        assert np.array_equal(b1[key], b2[key])
