@@ -17,9 +17,9 @@ MUTANTS = [
     ("dropped_head", "    acc += wt[h] * relu;\n", "    acc += h + 1 < H ? wt[h] * relu : 0.0f;\n"),
     ("ties_high_pos", "return (x->pos > y->pos) - (x->pos < y->pos);",
      "return (x->pos < y->pos) - (x->pos > y->pos);"),
-    ("no_k_scale", "p->kf[(size_t)s * d + i] = p->dtype == ORACLE_E4M3 ? v * scale : v;",
+    ("no_k_scale", "p->kf[(size_t)s * d + i] = kd == ORACLE_E4M3 ? v * scale : v;",
      "p->kf[(size_t)s * d + i] = v;"),
-    ("no_q_scale", "qT[(size_t)i * p->H + h] = p->dtype == ORACLE_E4M3 ? v * scale : v;",
+    ("no_q_scale", "qT[(size_t)i * p->H + h] = qd == ORACLE_E4M3 ? v * scale : v;",
      "qT[(size_t)i * p->H + h] = v;"),
     ("transposed_q", "size_t at = ((size_t)t * p->H + h) * p->d + i;",
      "size_t at = (size_t)t * p->H * p->d + ((size_t)i * p->H + h) % ((size_t)p->H * p->d);"),
@@ -43,8 +43,8 @@ MUTANTS = [
     ("bwd_dw_no_relu", "dw[t * H + h] += g * relu;", "dw[t * H + h] += g * x;"),
     ("bwd_mask_at_zero", "if (x > 0.0) {\n              dqt[e]", "if (x >= 0.0) {\n              dqt[e]"),
     ("bwd_wrong_key_row", "size_t e = (size_t)s * d + i;", "size_t e = (size_t)((s + 1) % L) * d + i;"),
-    ("bwd_no_k_scale", "double v = (double)element(k, dtype, (size_t)s * d + i) * scale;",
-     "double v = (double)element(k, dtype, (size_t)s * d + i);"),
+    ("bwd_no_k_scale", "double v = (double)element(k, k_dtype(dtype), (size_t)s * d + i) * scale;",
+     "double v = (double)element(k, k_dtype(dtype), (size_t)s * d + i);"),
     ("bwd_grad_row", "double g = (double)grad[t * k_top + j];\n        const double* ks = kd + (size_t)s * d;\n        for (int h = 0; h < H; ++h) {\n          double x = 0.0;\n          for (int i = 0; i < d; ++i) x += qd[(size_t)h * d + i] * ks[i];\n          int amb = fabs(x) <= eps * qnorm[h] * knorm[s];\n          double relu",
      "double g = (double)grad[((t + 1) % n) * k_top + j];\n        const double* ks = kd + (size_t)s * d;\n        for (int h = 0; h < H; ++h) {\n          double x = 0.0;\n          for (int i = 0; i < d; ++i) x += qd[(size_t)h * d + i] * ks[i];\n          int amb = fabs(x) <= eps * qnorm[h] * knorm[s];\n          double relu"),
 ]
