@@ -27,7 +27,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
 DEV_REPLAY_BAD_INDEX = 0x1
 DEV_BAD_SCALE = 0x2
 DEV_BAD_POSITION = 0x4
-BF16, E4M3 = 0, 1
+BF16, E4M3, E4M3_BF16 = 0, 1, 2  # E4M3_BF16: e4m3 q (with q_scale), bf16 k
 
 # the C-ABI symbols declared in include/hytopk.h
 symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", "hytopk_replay",
@@ -114,9 +114,11 @@ def _dtype_code(q, k):
         raise TypeError("q and k must be bfloat16 (or its 16-bit patterns) or float8_e4m3fn "
                         "(or its 8-bit codes)")
     dq, dk = kinds[q.dtype], kinds[k.dtype]
-    if dq != dk:
-        raise TypeError("q and k must have the same element type")
-    return dq
+    if dq == dk:
+        return dq
+    if dq == E4M3 and dk == BF16:
+        return E4M3_BF16
+    raise TypeError("bf16 q with e4m3 k is not supported (e4m3 q with bf16 k is)")
 
 
 def _ptr(t):

@@ -15,12 +15,15 @@ constexpr int kVersion = 100;  // 0.1.0
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool supported_h(int H) { return H >= 1 && H <= 128 && (H & (H - 1)) == 0; }
-// rows of 64, 128 or 256 bytes: bf16 d = 32, 64, 128; e4m3 d = 64, 128, 256
+// key rows of 64, 128 or 256 bytes: bf16 keys d = 32, 64, 128; e4m3 keys d = 64, 128, 256
 bool supported_d(int d, hytopk_dtype dt) {
-  return dt == HYTOPK_BF16 ? (d == 32 || d == 64 || d == 128) : (d == 64 || d == 128 || d == 256);
+  return dt != HYTOPK_E4M3 ? (d == 32 || d == 64 || d == 128) : (d == 64 || d == 128 || d == 256);
 }
-int elem_size(hytopk_dtype dt) { return dt == HYTOPK_BF16 ? 2 : 1; }
-bool valid_dtype(hytopk_dtype dt) { return dt == HYTOPK_BF16 || dt == HYTOPK_E4M3; }
+// bytes of a key element (also of the packed query operand, which takes the key type)
+int elem_size(hytopk_dtype dt) { return dt == HYTOPK_E4M3 ? 1 : 2; }
+bool valid_dtype(hytopk_dtype dt) {
+  return dt == HYTOPK_BF16 || dt == HYTOPK_E4M3 || dt == HYTOPK_E4M3_BF16;
+}
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int pad_queries(int n) { return (n + kQueryPad - 1) / kQueryPad * kQueryPad; }
@@ -73,6 +76,7 @@ Problem make_problem(const void* q, const float* q_scale, const void* k, const f
   p.d = d;
   p.k_top = k_top;
   p.dt = dt == HYTOPK_E4M3 ? 1 : 0;
+  p.qdt = dt == HYTOPK_BF16 ? 0 : 1;
   return p;
 }
 
@@ -104,11 +108,10 @@ hytopk_status check_inputs(const void* q, const float* q_scale, const void* k, c
                            const float* w, hytopk_dtype dt, int n) {
   if (!k) return HYTOPK_INVALID_ARG;
   if (n > 0 && (!q || !w)) return HYTOPK_INVALID_ARG;
-  if (dt == HYTOPK_E4M3) {
-    if (!k_scale || (n > 0 && !q_scale)) return HYTOPK_INVALID_ARG;
-  } else if (q_scale || k_scale) {
-    return HYTOPK_INVALID_ARG;
-  }
+  // e4m3 rows carry a scale, bf16 rows none
+  const bool q_e4m3 = dt != HYTOPK_BF16, k_e4m3 = dt == HYTOPK_E4M3;
+  if (q_e4m3 ? (n > 0 && !q_scale) : (q_scale != nullptr)) return HYTOPK_INVALID_ARG;
+  if (k_e4m3 ? !k_scale : (k_scale != nullptr)) return HYTOPK_INVALID_ARG;
   const void* ptrs[] = {q, q_scale, k, k_scale, w};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return HYTOPK_MISALIGNED;
@@ -219,15 +222,20 @@ static size_t twopass_lists_bytes(int L) { return align_up((size_t)kRecoveryCtas
 static size_t twopass_weights_bytes(int n, int H) {
   return align_up(((size_t)n + kQueryPad) * H * 4, 1024);
 }
-static size_t twopass_fixed_bytes(int n, int L, int H) {
-  return twopass_lists_bytes(L) + twopass_weights_bytes(n, H);
+// e4m3 q against bf16 k: the table kernel reads q through a tensor map in the
+// key element type, so q is first converted to a bf16 copy [n, H, d]
+static size_t twopass_qconv_bytes(int n, int H, int d, hytopk_dtype dt) {
+  return dt == HYTOPK_E4M3_BF16 ? align_up((size_t)n * H * d * 2, 1024) : 0;
+}
+static size_t twopass_fixed_bytes(int n, int L, int H, int d, hytopk_dtype dt) {
+  return twopass_lists_bytes(L) + twopass_weights_bytes(n, H) + twopass_qconv_bytes(n, H, d, dt);
 }
 
 size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,
                                      int rows_per_chunk) {
   if (check_shape(n, L, H, d, k_top, dt) != HYTOPK_OK) return 0;
   const int rows = rows_per_chunk <= 0 ? (n > 0 ? n : 1) : rows_per_chunk;
-  return twopass_fixed_bytes(n, L, H) + align_up((size_t)rows * L * 4, 1024);
+  return twopass_fixed_bytes(n, L, H, d, dt) + align_up((size_t)rows * L * 4, 1024);
 }
 
 hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const void* k,
@@ -243,7 +251,7 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
   if (n == 0) return HYTOPK_OK;
   if (!positions || !idx_out || !workspace) return HYTOPK_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HYTOPK_MISALIGNED;
-  const size_t fixed = twopass_fixed_bytes(n, L, H);
+  const size_t fixed = twopass_fixed_bytes(n, L, H, d, dt);
   const size_t row_bytes = (size_t)L * 4;
   if (workspace_bytes < fixed + row_bytes) return HYTOPK_WORKSPACE_TOO_SMALL;
   size_t chunk = (workspace_bytes - fixed) / row_bytes;
@@ -252,8 +260,15 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
   uint64_t* lists = reinterpret_cast<uint64_t*>(base);
   float* hw = reinterpret_cast<float*>(base + twopass_lists_bytes(L));
   float* table = reinterpret_cast<float*>(base + fixed);
-  const Problem p = make_problem(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt);
-  HYTOPK_TRY(launch_fold_weights(p, n + kQueryPad, hw, stream));
+  const Problem p0 = make_problem(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt);
+  HYTOPK_TRY(launch_fold_weights(p0, n + kQueryPad, hw, stream));  // folds q_scale
+  Problem p = p0;
+  if (dt == HYTOPK_E4M3_BF16) {
+    void* qconv = base + twopass_lists_bytes(L) + twopass_weights_bytes(n, H);
+    HYTOPK_TRY(launch_convert_queries(p0, qconv, stream));
+    p.q = qconv;
+    p.qdt = 0;
+  }
   for (int row0 = 0; row0 < n; row0 += (int)chunk) {
     const int rows = (int)((size_t)(n - row0) < chunk ? (size_t)(n - row0) : chunk);
     HYTOPK_TRY(launch_table(p, row0, rows, table, hw, dev_status, stream));

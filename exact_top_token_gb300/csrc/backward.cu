@@ -40,9 +40,10 @@ extern "C" hytopk_status hytopk_replay_backward(const void* q, const float* q_sc
   a.n = n;
   a.L = L;
   a.k_top = k_top;
+  a.q_e4m3 = dt != HYTOPK_BF16;
   a.status = dev_status;
   const int grid = n < num_sms() ? n : num_sms();
-  const cudaError_t e = dt == HYTOPK_BF16 ? launch_backward_bf16(d, H, a, grid, stream)
-                                          : launch_backward_e4m3(d, H, a, grid, stream);
+  const cudaError_t e = dt == HYTOPK_E4M3 ? launch_backward_e4m3(d, H, a, grid, stream)
+                                          : launch_backward_bf16(d, H, a, grid, stream);
   return e == cudaSuccess ? HYTOPK_OK : HYTOPK_CUDA_ERROR;
 }

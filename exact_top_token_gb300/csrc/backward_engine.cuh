@@ -66,6 +66,7 @@ struct BArgs {
   float* dk;
   float* dw;
   int n, L, k_top;
+  int q_e4m3;  // q rows are e4m3 codes with q_scale (keys may be bf16)
   uint32_t* status;
 };
 
@@ -307,12 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
       const bool ok = tc::mbar_wait(q_empty + qb, ((qi >> 1) & 1) ^ 1, abort_flag, a.status);
       if (!__all_sync(0xffffffffu, ok)) return false;
       uint8_t* qd = q_buf(qb);
-      constexpr int QCH = D * C_::ES / 16;  // 16-byte source chunks per q row
-      for (int f = tid; f < H * QCH; f += kProducers) {
-        const int h = f / QCH, cq = f - h * QCH;
+      const bool q8 = DT == 1 || a.q_e4m3;  // q rows of e4m3 codes
+      const int qes = q8 ? 1 : 2;
+      const int qch = D * qes / 16;  // 16-byte source chunks per q row
+      for (int f = tid; f < H * qch; f += kProducers) {
+        const int h = f / qch, cq = f - h * qch;
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-            static_cast<const uint8_t*>(a.q) + ((size_t)t * H + h) * D * C_::ES) + cq);
-        if (DT == 0) {
+            static_cast<const uint8_t*>(a.q) + ((size_t)t * H + h) * D * qes) + cq);
+        if (!q8) {
           *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 8, H)) = v;
         } else {
           uint4 lo, hi;
@@ -325,12 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
       uint32_t* pairs = reinterpret_cast<uint32_t*>(wsq + 2 * H);
       for (int h = tid; h < H; h += kProducers) {
         wsq[h] = a.w[(size_t)t * H + h];
-        wsq[H + h] = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+        wsq[H + h] = q8 ? a.q_scale[(size_t)t * H + h] : 1.0f;
       }
       for (int pr = tid; pr < H / 2; pr += kProducers) {
         const int h = 2 * pr;
-        const float s0 = DT == 1 ? a.q_scale[(size_t)t * H + h] : 1.0f;
-        const float s1 = DT == 1 ? a.q_scale[(size_t)t * H + h + 1] : 1.0f;
+        const float s0 = q8 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+        const float s1 = q8 ? a.q_scale[(size_t)t * H + h + 1] : 1.0f;
         uint16_t h0, l0, h1, l1;
         split_bf16(a.w[(size_t)t * H + h] * s0, h0, l0);
         split_bf16(a.w[(size_t)t * H + h + 1] * s1, h1, l1);

@@ -48,7 +48,9 @@ struct Problem {
   const float* k_scale;
   const float* w;
   const int32_t* positions;
-  int n, L, H, d, k_top, dt;  // dt: 0 bf16, 1 e4m3
+  int n, L, H, d, k_top;
+  int dt;   // key elements (and the packed query operand): 0 bf16, 1 e4m3
+  int qdt;  // query elements as given: 0 bf16, 1 e4m3 (with q_scale)
 };
 
 // Workspace of hytopk_select, carved by the host.
@@ -119,6 +121,27 @@ __device__ __forceinline__ float load_elem(const void* base, size_t i) {
 __device__ __forceinline__ float finish_score(float acc, float ks) {
   float s = acc * ks;
   return s == 0.0f ? 0.0f : s;
+}
+
+// 8 e4m3 codes -> 8 bf16 (exact: every e4m3 value is a bf16 value)
+__device__ __forceinline__ uint4 e4m3x8_to_bf16(uint2 in) {
+  const uint32_t w[2] = {in.x, in.y};
+  uint32_t out[4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint16_t two = (uint16_t)(w[i] >> (16 * h));
+      uint32_t h2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+      const float f0 = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+      const float f1 = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+      uint32_t b2;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(b2) : "f"(f1), "f"(f0));
+      out[2 * i + h] = b2;
+    }
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // ---- ordered keys -------------------------------------------------------------------

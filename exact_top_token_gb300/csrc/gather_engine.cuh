@@ -68,6 +68,7 @@ struct GArgs {
   // replay: original queries
   const void* q;
   const float* q_scale;
+  int q_e4m3;  // replay: q rows are e4m3 codes (converted to the bf16 operand)
   const float* w;
   const int32_t* idx;
   float* out;
@@ -188,20 +189,30 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
 
     // ---- the query operand (H rows of d, zero-padded to NQ) and weights ----
     {
+      // e4m3 queries against bf16 keys (replay only; the other modes read the
+      // packed operand): D-byte rows, 8 codes per 16-byte chunk of the operand
+      const bool q8 = DT == 0 && MODE == kReplay && a.q_e4m3;
+      const int q_row_bytes = q8 ? D : RB;
       const uint8_t* qsrc =
-          MODE == kReplay ? reinterpret_cast<const uint8_t*>(a.q) + (size_t)t * H * RB
+          MODE == kReplay ? reinterpret_cast<const uint8_t*>(a.q) + (size_t)t * H * q_row_bytes
                           : reinterpret_cast<const uint8_t*>(a.qp) + (size_t)slot * H * RB;
       for (int f = threadIdx.x; f < NQ * CPR; f += kThreads) {
         const int row = f / CPR, c = f % CPR;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < H) v = *reinterpret_cast<const uint4*>(qsrc + (size_t)row * RB + c * 16);
+        if (row < H) {
+          if (q8)
+            v = e4m3x8_to_bf16(
+                *reinterpret_cast<const uint2*>(qsrc + (size_t)row * q_row_bytes + c * 8));
+          else
+            v = *reinterpret_cast<const uint4*>(qsrc + (size_t)row * RB + c * 16);
+        }
         *reinterpret_cast<uint4*>(qbuf + Geo::chunk_offset(row, c, NQ)) = v;
       }
       for (int h = threadIdx.x; h < H; h += kThreads) {
         float hw;  // halved folded weight, as in the prep kernel
         if (MODE == kReplay) {
           float wv = a.w[(size_t)t * H + h];
-          if (DT == 1) wv *= a.q_scale[(size_t)t * H + h];
+          if (DT == 1 || a.q_e4m3) wv *= a.q_scale[(size_t)t * H + h];
           hw = 0.5f * wv;
         } else {
           hw = a.wq[(size_t)slot * H + h];

@@ -86,6 +86,7 @@ cudaError_t launch_replay(const Problem& p, const int32_t* idx, float* out, uint
   gather::GArgs a = base_args(p);
   a.q = p.q;
   a.q_scale = p.q_scale;
+  a.q_e4m3 = p.qdt == 1 && p.dt == 0;
   a.w = p.w;
   a.idx = idx;
   a.out = out;

@@ -12,6 +12,8 @@ namespace hytopk {
 // prep.cu
 cudaError_t launch_prep(const Problem& p, const SelectWs& ws, cudaStream_t st);
 cudaError_t launch_fold_weights(const Problem& p, int rows, float* hw, cudaStream_t st);
+// e4m3 q -> bf16 copy [n, H, d] (the mixed dtype's paths that read q as given)
+cudaError_t launch_convert_queries(const Problem& p, void* out, cudaStream_t st);
 
 // score_*.cu: the scoring phases
 cudaError_t launch_threshold(const Problem& p, const SelectWs& ws, const float* override_thr,

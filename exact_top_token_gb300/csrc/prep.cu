@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(1024) k_rank_by_position(const int32_t* __rest
   if (t < n) perm[rank] = t;
 }
 
+// Slot row of the packed query operand, in the key element type: a copy, or
+// (e4m3 queries against bf16 keys) an exact conversion to bf16.
 __global__ void __launch_bounds__(128) k_pack_queries(Problem p, SelectWs ws) {
   const int slot = blockIdx.x;
   const int t = slot < p.n ? ws.perm[slot] : -1;
@@ -61,12 +63,18 @@ __global__ void __launch_bounds__(128) k_pack_queries(Problem p, SelectWs ws) {
     }
     return;
   }
-  const uint4* src =
-      reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.q) + (size_t)t * row_bytes);
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = src[v];
+  if (p.qdt == p.dt) {
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.q) +
+                                                      (size_t)t * row_bytes);
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = src[v];
+  } else {  // e4m3 -> bf16: 8 codes in, 16 bytes out
+    const uint2* src = reinterpret_cast<const uint2*>(reinterpret_cast<const uint8_t*>(p.q) +
+                                                      (size_t)t * p.H * p.d);
+    for (int v = threadIdx.x; v < nvec; v += blockDim.x) dst[v] = e4m3x8_to_bf16(src[v]);
+  }
   for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
     float wv = p.w[(size_t)t * p.H + h];
-    if (p.dt == 1) {
+    if (p.qdt == 1) {
       const float qs = p.q_scale[(size_t)t * p.H + h];
       if (!(qs > 0.0f)) set_status(ws.counters, HYTOPK_DEV_BAD_SCALE);
       wv *= qs;
@@ -97,13 +105,29 @@ __global__ void k_fold_weights(Problem p, int rows, float* __restrict__ hw) {
     float wv = 0.0f;
     if (t < (size_t)p.n) {
       wv = p.w[i];
-      if (p.dt == 1) wv *= p.q_scale[i];
+      if (p.qdt == 1) wv *= p.q_scale[i];
     }
     hw[i] = 0.5f * wv;
   }
 }
 
+// q [n, H, d] e4m3 codes -> bf16 (exact), for paths that read q as given
+__global__ void k_convert_queries(const uint2* __restrict__ q8, size_t n_chunks,
+                                  uint4* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n_chunks;
+       i += (size_t)gridDim.x * blockDim.x)
+    out[i] = e4m3x8_to_bf16(q8[i]);
+}
+
 }  // namespace
+
+cudaError_t launch_convert_queries(const Problem& p, void* out, cudaStream_t st) {
+  const size_t n_chunks = (size_t)p.n * p.H * p.d / 8;
+  if (n_chunks == 0) return cudaSuccess;
+  k_convert_queries<<<512, 256, 0, st>>>(reinterpret_cast<const uint2*>(p.q), n_chunks,
+                                         reinterpret_cast<uint4*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fold_weights(const Problem& p, int rows, float* hw, cudaStream_t st) {
   k_fold_weights<<<256, 256, 0, st>>>(p, rows, hw);

@@ -178,7 +178,7 @@ extern "C" hytopk_status hytopk_select_sharded(const void* q, const float* q_sca
 
   const int S = shard_keys(L, P);
   const int used = (L + S - 1) / S;
-  const int esize = dt == HYTOPK_BF16 ? 2 : 1;
+  const int esize = dt == HYTOPK_E4M3 ? 1 : 2;  // key element bytes
   if (cudaMemsetAsync(status, 0, 4, stream) != cudaSuccess) return HYTOPK_CUDA_ERROR;
   const int pos_blocks = (n + 255) / 256;
   const size_t entries = (size_t)n * k_top;

@@ -40,15 +40,19 @@
  *   - Layouts are row-major and contiguous:
  *       q        [n, H, d] elements of `dt`
  *       q_scale  [n, H]    fp32, one scale per (query, head) row of d elements;
- *                          required for HYTOPK_E4M3, must be NULL for bf16
+ *                          required when q is e4m3 (HYTOPK_E4M3 and
+ *                          HYTOPK_E4M3_BF16), must be NULL for bf16 q
  *       k        [L, d]    elements of `dt`
- *       k_scale  [L]       fp32 per key row; required for e4m3, NULL for bf16
+ *       k_scale  [L]       fp32 per key row; required for e4m3 k (HYTOPK_E4M3),
+ *                          NULL for bf16 k (HYTOPK_BF16 and HYTOPK_E4M3_BF16)
  *       w        [n, H]    fp32 head weights (any sign)
  *       positions[n]       int32, 0 <= pos < L, any order
  *     e4m3 is OCP FP8 E4M3 ("fn"); an element's value is code * scale. Scales
  *     must be finite and > 0 (then ReLU(a*x) = a*ReLU(x) and scales may be
  *     applied after the dot); a non-positive scale sets HYTOPK_DEV_BAD_SCALE.
  *     Inputs must be finite.
+ *     HYTOPK_E4M3_BF16 converts q to bf16 exactly (every e4m3 value is a bf16
+ *     value) and runs the bf16 path; q_scale is folded into w as for e4m3.
  *   - Supported shapes: H in {1,2,4,8,16,32,64,128}; key rows of 64, 128 or
  *     256 bytes, i.e. d in {32, 64, 128} for bf16 and d in {64, 128, 256} for
  *     e4m3; 1 <= k_top <= 16384; n >= 0; L >= 1 (hytopk_replay_backward:
@@ -87,7 +91,9 @@ typedef enum {
   HYTOPK_MISALIGNED = 5            /* a device pointer is not 16-byte aligned */
 } hytopk_status;
 
-typedef enum { HYTOPK_BF16 = 0, HYTOPK_E4M3 = 1 } hytopk_dtype;
+/* Element types of q and k: both bf16, both e4m3 (with q_scale and k_scale),
+ * or e4m3 q (with q_scale) and bf16 k (no k_scale). */
+typedef enum { HYTOPK_BF16 = 0, HYTOPK_E4M3 = 1, HYTOPK_E4M3_BF16 = 2 } hytopk_dtype;
 
 /* Device status bits (written with atomicOr on the device). */
 #define HYTOPK_DEV_REPLAY_BAD_INDEX 0x1u /* replay index not -1 and outside [0, L): entry is NaN */

@@ -81,6 +81,10 @@ def test_host_checks_reject_bad_arguments(lib):
     assert call(d=256) == 2  # bf16 rows of 512 bytes
     assert call(k_top=20000) == 2
     assert call(dt=1) == 1  # e4m3 needs scales
+    assert call(dt=2) == 1  # e4m3 q needs q_scale
+    assert call(dt=2, qs=fake, ks=fake) == 1  # bf16 k takes no k_scale
+    assert call(dt=2, qs=fake, wsb=16) == 3  # accepted up to the workspace check
+    assert call(dt=3) == 1
     assert call(qs=fake) == 1  # bf16 takes no scales
     assert call(cap=4) == 1  # capacity < k
     assert call(wsb=16) == 3

@@ -53,17 +53,18 @@ def int_case(L, n, H, d, k_top, dtype, seed):
     g = si.rng_for(seed)
     case = si.random_case(L, n, H, d, k_top, "bf16", seed, "last", "int")
     case["w"] = g.integers(-2, 3, size=(n, H)).astype(np.float32)
-    if dtype == "e4m3":
+    if dtype in ("e4m3", "e4m3_bf16"):
         # integer codes 1..3 in e4m3 with power-of-two scales: exact everywhere
-        qf = g.integers(-3, 4, size=(n, H, d)).astype(np.float32)
-        kf = g.integers(-3, 4, size=(L, d)).astype(np.float32)
         import torch
 
+        qf = g.integers(-3, 4, size=(n, H, d)).astype(np.float32)
         case["q"] = torch.from_numpy(qf).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-        case["k"] = torch.from_numpy(kf).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
         case["q_scale"] = np.exp2(g.integers(-2, 2, size=(n, H))).astype(np.float32)
-        case["k_scale"] = np.exp2(g.integers(-2, 2, size=L)).astype(np.float32)
-        case["dtype"] = "e4m3"
+        if dtype == "e4m3":
+            kf = g.integers(-3, 4, size=(L, d)).astype(np.float32)
+            case["k"] = torch.from_numpy(kf).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            case["k_scale"] = np.exp2(g.integers(-2, 2, size=L)).astype(np.float32)
+        case["dtype"] = dtype
     return case, g
 
 
@@ -72,6 +73,7 @@ def int_case(L, n, H, d, k_top, dtype, seed):
     (3000, 40, 32, 128, 300, "bf16"),
     (2048, 33, 64, 128, 200, "e4m3"),
     (1500, 20, 16, 64, 129, "e4m3"),
+    (1800, 24, 32, 128, 160, "e4m3_bf16"),
 ])
 def test_integer_data_bit_exact(hk, dev, L, n, H, d, k_top, dtype):
     case, g = int_case(L, n, H, d, k_top, dtype, seed=L + n + H)
@@ -95,6 +97,7 @@ def within(gpu, ref, name, rtol=2e-4, eps_amb=True):
     (5000, 48, 32, 128, 512, "bf16"),
     (8192, 40, 64, 128, 1024, "e4m3"),
     (3000, 70, 16, 64, 300, "e4m3"),
+    (4000, 30, 64, 128, 400, "e4m3_bf16"),
 ])
 def test_random_data_within_tolerance(hk, dev, L, n, H, d, k_top, dtype):
     case = si.random_case(L, n, H, d, k_top, dtype, seed=7 + n, positions="random")

@@ -88,6 +88,8 @@ def test_recovery_stress_full_fallback(hk, dev):
     (4000, 50, 16, 32, 256, "bf16", "random"),     # 64-byte bf16 rows
     (6000, 40, 64, 256, 300, "e4m3", "random"),    # 256-byte e4m3 rows
     (300, 9, 8, 256, 500, "e4m3", "last"),         # ctx < k
+    (5000, 40, 32, 128, 256, "e4m3_bf16", "random"),  # e4m3 q, bf16 k
+    (3000, 30, 16, 64, 200, "e4m3_bf16", "last"),
 ])
 def test_random_small(hk, dev, L, n, H, d, k_top, dt, pos):
     case = si.random_case(L, n, H, d, k_top, dt, seed=L + n, positions=pos)
@@ -297,3 +299,20 @@ def test_twopass_exact_on_integer_data(hk, dev):
     t = si.to_torch(case, dev)
     i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], case["k_top"])
     compare(case, np.arange(64), i2.cpu().numpy(), s2.cpu().numpy(), exact=True)
+
+
+def test_mixed_q_e4m3_k_bf16_paths_agree(hk, dev):
+    """e4m3 q with bf16 k: the selection matches the oracle, and replay, the
+    two-pass path and the key-sharded selection return its scores bit for bit."""
+    case = si.random_case(6000, 48, 64, 128, 300, "e4m3_bf16", seed=41, positions="random")
+    idx, sc, st, t = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(48), gi, gs)
+    assert hk.read_stats(st)["device_status"] == 0
+    rs = hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"])
+    assert np.array_equal(rs.cpu().numpy(), gs)
+    i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], 300, q_scale=t["q_scale"])
+    assert np.array_equal(i2.cpu().numpy(), gi) and np.array_equal(s2.cpu().numpy(), gs)
+    i3, s3, _ = hk.select_sharded(t["q"], t["k"], t["w"], t["positions"], 300, 3,
+                                  q_scale=t["q_scale"])
+    assert np.array_equal(i3.cpu().numpy(), gi) and np.array_equal(s3.cpu().numpy(), gs)
