@@ -17,13 +17,14 @@ import os
 from . import _build
 
 __all__ = ["build", "load", "select", "select_twopass", "replay", "select_workspace_size",
+           "select_sharded", "select_varlen", "replay_varlen", "replay_backward",
            "twopass_workspace_size", "HytopkError", "STATUS", "PHASES", "Stats",
            "symbols"]
 
 MAX_RECOVERY_ROWS = 64
 PHASES = ("prep", "threshold", "filter", "check", "select", "recover")
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
-          3: "workspace too small", 4: "CUDA error", 5: "device pointer not 16-byte aligned"}
+          3: "workspace too small", 4: "CUDA error", 5: "device pointer misaligned"}
 DEV_REPLAY_BAD_INDEX = 0x1
 DEV_BAD_SCALE = 0x2
 DEV_BAD_POSITION = 0x4
@@ -33,7 +34,8 @@ BF16, E4M3, E4M3_BF16 = 0, 1, 2  # E4M3_BF16: e4m3 q (with q_scale), bf16 k
 symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", "hytopk_replay",
            "hytopk_twopass_workspace_size", "hytopk_select_twopass", "hytopk_select_noalloc",
            "hytopk_select_sharded_workspace_size", "hytopk_select_sharded",
-           "hytopk_replay_backward",
+           "hytopk_replay_backward", "hytopk_select_varlen_workspace_size",
+           "hytopk_select_varlen", "hytopk_replay_varlen",
            "hytopk_status_string", "hytopk_version")
 
 
@@ -94,6 +96,13 @@ def load(path: str | None = None):
                                           P]
     lib.hytopk_replay_backward.restype = I
     lib.hytopk_replay_backward.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]
+    lib.hytopk_select_varlen_workspace_size.restype = Z
+    lib.hytopk_select_varlen_workspace_size.argtypes = [P, P, I, I, I, I, I, I]
+    lib.hytopk_select_varlen.restype = I
+    lib.hytopk_select_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, I, P, Z, P,
+                                         P]
+    lib.hytopk_replay_varlen.restype = I
+    lib.hytopk_replay_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]
     lib.hytopk_status_string.restype = ctypes.c_char_p
     lib.hytopk_status_string.argtypes = [I]
     lib.hytopk_version.restype = I
@@ -258,6 +267,83 @@ def select_sharded(q, k, w, positions, k_top, num_shards, *, q_scale=None, k_sca
     if status != 0:
         raise HytopkError(status, "hytopk_select_sharded")
     return idx, sc, st
+
+
+def _offsets(cu, name):
+    """Host int32 copy of a B+1 offset array (list, numpy or tensor)."""
+    import numpy as np
+
+    if hasattr(cu, "cpu"):
+        cu = cu.cpu().numpy()
+    a = np.ascontiguousarray(np.asarray(cu, dtype=np.int32))
+    if a.ndim != 1 or a.size < 2:
+        raise ValueError(f"{name} must hold B+1 offsets")
+    return a
+
+
+def _cu_ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def select_varlen_workspace_size(cu_q, cu_k, H, d, k_top, capacity=0, dtype=BF16) -> int:
+    cq, ck = _offsets(cu_q, "cu_q"), _offsets(cu_k, "cu_k")
+    if cq.size != ck.size:
+        raise ValueError("cu_q and cu_k must have the same length")
+    return int(load().hytopk_select_varlen_workspace_size(_cu_ptr(cq), _cu_ptr(ck), cq.size - 1, H,
+                                                          d, k_top, capacity, dtype))
+
+
+def select_varlen(q, k, w, positions, cu_q, cu_k, k_top, *, q_scale=None, k_scale=None,
+                  capacity=0, scores=True, stats=False, workspace=None, stream=None):
+    """Packed variable-length batch: sequence b owns queries cu_q[b]:cu_q[b+1]
+    and keys cu_k[b]:cu_k[b+1]; positions and returned indices are relative to
+    the sequence. Same outputs as :func:`select` over the concatenated rows."""
+    import torch
+
+    lib = load()
+    dt, n, L, H, d, dev = _common(q, q_scale, k, k_scale, w)
+    _check_tensor("positions", positions, dev, torch.int32, (n,))
+    cq, ck = _offsets(cu_q, "cu_q"), _offsets(cu_k, "cu_k")
+    if cq.size != ck.size or cq[-1] != n or ck[-1] != L:
+        raise ValueError("cu_q / cu_k do not match the query and key counts")
+    B = cq.size - 1
+    idx = torch.empty((n, k_top), dtype=torch.int32, device=dev)
+    sc = torch.empty((n, k_top), dtype=torch.float32, device=dev) if scores else None
+    need = lib.hytopk_select_varlen_workspace_size(_cu_ptr(cq), _cu_ptr(ck), B, H, d, k_top,
+                                                   capacity, dt)
+    if need == 0:
+        raise HytopkError(2, "hytopk_select_varlen_workspace_size")
+    ws = _workspace(need, dev, workspace)
+    st = torch.zeros(8, dtype=torch.int32, device=dev) if stats else None
+    status = lib.hytopk_select_varlen(
+        _ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(positions), _cu_ptr(cq),
+        _cu_ptr(ck), B, H, d, k_top, dt, _ptr(idx), _ptr(sc), capacity, _ptr(ws), ws.numel(),
+        _ptr(st), _stream(dev, stream))
+    if status != 0:
+        raise HytopkError(status, "hytopk_select_varlen")
+    return idx, sc, st
+
+
+def replay_varlen(q, k, w, idx, cu_q, cu_k, *, q_scale=None, k_scale=None, status=None,
+                  stream=None):
+    """Selection replay over a packed variable-length batch (indices relative
+    to each query's sequence)."""
+    import torch
+
+    lib = load()
+    dt, n, L, H, d, dev = _common(q, q_scale, k, k_scale, w)
+    k_top = idx.shape[1]
+    _check_tensor("idx", idx, dev, torch.int32, (n, k_top))
+    cq, ck = _offsets(cu_q, "cu_q"), _offsets(cu_k, "cu_k")
+    if cq.size != ck.size or cq[-1] != n or ck[-1] != L:
+        raise ValueError("cu_q / cu_k do not match the query and key counts")
+    res = torch.empty((n, k_top), dtype=torch.float32, device=dev)
+    st = lib.hytopk_replay_varlen(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w),
+                                  _ptr(idx), _cu_ptr(cq), _cu_ptr(ck), cq.size - 1, H, d, k_top,
+                                  dt, _ptr(res), _ptr(status), _stream(dev, stream))
+    if st != 0:
+        raise HytopkError(st, "hytopk_replay_varlen")
+    return res
 
 
 def read_stats(st) -> dict:

@@ -112,9 +112,11 @@ hytopk_status check_inputs(const void* q, const float* q_scale, const void* k, c
   const bool q_e4m3 = dt != HYTOPK_BF16, k_e4m3 = dt == HYTOPK_E4M3;
   if (q_e4m3 ? (n > 0 && !q_scale) : (q_scale != nullptr)) return HYTOPK_INVALID_ARG;
   if (k_e4m3 ? !k_scale : (k_scale != nullptr)) return HYTOPK_INVALID_ARG;
-  const void* ptrs[] = {q, q_scale, k, k_scale, w};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return HYTOPK_MISALIGNED;
+  // rows are read in 16-byte pieces; scales and weights one fp32 at a time
+  if ((q && !aligned16(q)) || !aligned16(k)) return HYTOPK_MISALIGNED;
+  const float* fptrs[] = {q_scale, k_scale, w};
+  for (const float* p : fptrs)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u) != 0) return HYTOPK_MISALIGNED;
   return HYTOPK_OK;
 }
 
@@ -285,7 +287,7 @@ const char* hytopk_status_string(hytopk_status status) {
     case HYTOPK_UNSUPPORTED: return "unsupported shape or dtype";
     case HYTOPK_WORKSPACE_TOO_SMALL: return "workspace too small";
     case HYTOPK_CUDA_ERROR: return "CUDA error";
-    case HYTOPK_MISALIGNED: return "device pointer not 16-byte aligned";
+    case HYTOPK_MISALIGNED: return "device pointer misaligned";
   }
   return "unknown status";
 }

@@ -58,7 +58,9 @@
  *     e4m3; 1 <= k_top <= 16384; n >= 0; L >= 1 (hytopk_replay_backward:
  *     H in {16, 32, 64}, d in {64, 128}). Other shapes return
  *     HYTOPK_UNSUPPORTED.
- *   - Device pointers must be 16-byte aligned.
+ *   - q and k (and dq, dk of hytopk_replay_backward) must be 16-byte
+ *     aligned, every other array 4-byte aligned, so that an array offset by
+ *     whole rows stays a valid argument.
  *   - Scores are fp32. A selected score agrees with the definition above to
  *     within 1e-3 relative (exact for integer-valued data that fits fp32).
  */
@@ -88,7 +90,7 @@ typedef enum {
   HYTOPK_UNSUPPORTED = 2,          /* H, d or k_top outside the supported set */
   HYTOPK_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the *_workspace_size value */
   HYTOPK_CUDA_ERROR = 4,           /* a CUDA runtime call or launch failed */
-  HYTOPK_MISALIGNED = 5            /* a device pointer is not 16-byte aligned */
+  HYTOPK_MISALIGNED = 5            /* a device pointer breaks the alignment rules above */
 } hytopk_status;
 
 /* Element types of q and k: both bf16, both e4m3 (with q_scale and k_scale),
@@ -301,6 +303,44 @@ HYTOPK_API hytopk_status hytopk_select_sharded(const void* q, const float* q_sca
                                     float* scores_out, int capacity, void* workspace,
                                     size_t workspace_bytes, hytopk_stats* stats_out,
                                     cudaStream_t stream);
+
+/* Packed variable-length batches: B independent sequences whose queries and
+ * keys are concatenated, as in long-context training that packs several
+ * documents into one step. Sequence b owns the query rows
+ * [cu_q[b], cu_q[b+1]) and the key rows [cu_k[b], cu_k[b+1]); its queries'
+ * positions are relative to the sequence (0 <= pos < cu_k[b+1] - cu_k[b]) and
+ * select within it only, and the returned indices are relative to it too.
+ *   cu_q, cu_k: HOST arrays of B + 1 int32, non-decreasing, cu_q[0] = cu_k[0]
+ *   = 0, cu_q[B] = n, cu_k[B] = L. Every other argument is that of
+ *   hytopk_select over the whole packed arrays (idx_out, scores_out [n,
+ *   k_top]).
+ *   Each sequence runs the whole selection on its own rows, one after another
+ *   on `stream`, in one workspace of hytopk_select_varlen_workspace_size
+ *   bytes (the largest sequence's need). stats_out sums the sequences'
+ *   counts and ORs their status bits; n_queries = n.
+ *   Errors: as hytopk_select, plus HYTOPK_INVALID_ARG for inconsistent
+ *   cu_q / cu_k. */
+HYTOPK_API size_t hytopk_select_varlen_workspace_size(const int32_t* cu_q, const int32_t* cu_k,
+                                                      int B, int H, int d, int k_top,
+                                                      int capacity, hytopk_dtype dt);
+
+HYTOPK_API hytopk_status hytopk_select_varlen(const void* q, const float* q_scale, const void* k,
+                                              const float* k_scale, const float* w,
+                                              const int32_t* positions, const int32_t* cu_q,
+                                              const int32_t* cu_k, int B, int H, int d, int k_top,
+                                              hytopk_dtype dt, int32_t* idx_out,
+                                              float* scores_out, int capacity, void* workspace,
+                                              size_t workspace_bytes, hytopk_stats* stats_out,
+                                              cudaStream_t stream);
+
+/* Replay of a packed batch: idx [n, k_top] relative to each query's sequence
+ * (as hytopk_select_varlen returns them); otherwise as hytopk_replay. */
+HYTOPK_API hytopk_status hytopk_replay_varlen(const void* q, const float* q_scale, const void* k,
+                                              const float* k_scale, const float* w,
+                                              const int32_t* idx, const int32_t* cu_q,
+                                              const int32_t* cu_k, int B, int H, int d, int k_top,
+                                              hytopk_dtype dt, float* scores_out,
+                                              uint32_t* dev_status, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 HYTOPK_API const char* hytopk_status_string(hytopk_status status);

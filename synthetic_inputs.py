@@ -227,6 +227,28 @@ def subset(case, rows):
     return out
 
 
+def pack_varlen(cases):
+    """Concatenate independent cases (same H, d, dtype, k_top) into one packed
+    variable-length batch: returns (packed case, cu_q, cu_k), the offset arrays
+    holding B+1 entries. Positions stay relative to each sequence."""
+    first = cases[0]
+    cu_q = np.zeros(len(cases) + 1, np.int32)
+    cu_k = np.zeros(len(cases) + 1, np.int32)
+    for b, c in enumerate(cases):
+        assert c["dtype"] == first["dtype"] and c["k_top"] == first["k_top"]
+        cu_q[b + 1] = cu_q[b] + len(c["positions"])
+        cu_k[b + 1] = cu_k[b] + c["k"].shape[0]
+
+    def cat(key):
+        if first[key] is None:
+            return None
+        return np.ascontiguousarray(np.concatenate([c[key] for c in cases]))
+
+    out = {key: cat(key) for key in ("q", "q_scale", "k", "k_scale", "w", "positions")}
+    out.update(dtype=first["dtype"], k_top=first["k_top"], name=f"varlen_B{len(cases)}")
+    return out, cu_q, cu_k
+
+
 def sampled_rows(n: int, count: int = 64) -> np.ndarray:
     """A fixed subset of query rows: the first 16, the last 16 and the rest evenly spaced."""
     if n <= count:

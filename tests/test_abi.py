@@ -145,3 +145,56 @@ def test_backward_host_checks(lib):
     assert call(dt=1) == 1  # e4m3 needs scales
     assert call(dq=P((1 << 20) + 4)) == 5
     assert call(n=0, idx=None) == 0  # nothing to do
+
+
+def test_varlen_host_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def arr(*v):
+        return (ctypes.c_int32 * len(v))(*v)
+
+    ws = lib.hytopk_select_varlen_workspace_size
+    cq, ck = arr(0, 10, 10, 30), arr(0, 1000, 1500, 5000)
+    per = max(lib.hytopk_select_workspace_size(10, 1000, 4, 64, 64, 0, 0),
+              lib.hytopk_select_workspace_size(20, 3500, 4, 64, 64, 0, 0))
+    assert ws(cq, ck, 3, 4, 64, 64, 0, 0) >= per  # the largest sequence's workspace
+    assert ws(arr(0, 5, 3), arr(0, 10, 20), 2, 4, 64, 64, 0, 0) == 0  # decreasing offsets
+    assert ws(arr(1, 5), arr(0, 10), 1, 4, 64, 64, 0, 0) == 0  # not starting at 0
+    assert ws(arr(0, 5), arr(0, 0), 1, 4, 64, 64, 0, 0) == 0  # queries without keys
+    assert ws(cq, ck, 0, 4, 64, 64, 0, 0) == 0  # no sequence
+    assert ws(cq, ck, 3, 3, 64, 64, 0, 0) == 0  # H not a power of two
+
+    def call(**kw):
+        a = dict(q=fake, qs=None, k=fake, ks=None, w=fake, pos=fake, cq=cq, ck=ck, B=3, H=4, d=64,
+                 k_top=64, dt=0, idx=fake, sc=None, cap=0, ws=fake, wsb=1 << 34, st=None)
+        a.update(kw)
+        return lib.hytopk_select_varlen(a["q"], a["qs"], a["k"], a["ks"], a["w"], a["pos"],
+                                        a["cq"], a["ck"], a["B"], a["H"], a["d"], a["k_top"],
+                                        a["dt"], a["idx"], a["sc"], a["cap"], a["ws"], a["wsb"],
+                                        a["st"], None)
+
+    assert call(cq=arr(0, 10, 5, 30)) == 1
+    assert call(B=0) == 1
+    assert call(cq=None) == 1
+    assert call(H=6) == 2 and call(d=96) == 2
+    assert call(k=None) == 1 and call(pos=None) == 1
+    assert call(wsb=16) == 3
+    assert call(ws=P((1 << 20) + 128)) == 5
+    assert call(k=P((1 << 20) + 8)) == 5  # key rows must start 16-byte aligned
+    assert call(w=P((1 << 20) + 2)) == 5  # floats 4-byte aligned
+    assert call(dt=1) == 1  # e4m3 needs both scales
+    # a scale offset by one key passes the alignment check (then meets the small workspace)
+    assert call(dt=1, qs=fake, ks=P((1 << 20) + 4), wsb=16) == 3
+
+    def replay(**kw):
+        a = dict(q=fake, qs=None, k=fake, ks=None, w=fake, idx=fake, cq=cq, ck=ck, B=3, H=4,
+                 d=64, k_top=64, dt=0, sc=fake, st=None)
+        a.update(kw)
+        return lib.hytopk_replay_varlen(a["q"], a["qs"], a["k"], a["ks"], a["w"], a["idx"],
+                                        a["cq"], a["ck"], a["B"], a["H"], a["d"], a["k_top"],
+                                        a["dt"], a["sc"], a["st"], None)
+
+    assert replay(ck=arr(0, 1000, 900, 5000)) == 1
+    assert replay(idx=None) == 1 and replay(sc=None) == 1
+    assert replay(cq=arr(0, 0, 0, 0), ck=arr(0, 1, 2, 3)) == 0  # no query: nothing to do
