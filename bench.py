@@ -46,7 +46,7 @@ WORKLOADS = {"glm_1m": si.glm_1m, "mixed_contexts": si.mixed_contexts,
 # DRAM bytes (read + write) of one full-size filter launch, from the ncu
 # capture summarised in profiles/glm_1m_launch_list_tensorcore.txt. Must be
 # re-captured (or removed) whenever the filter kernel changes.
-FILTER_TRAFFIC_BYTES = {"glm_1m": 1.3667e9 + 0.4064e9}
+FILTER_TRAFFIC_BYTES = {"glm_1m": 1.2038e9 + 0.4013e9}
 
 
 def parse():
