@@ -41,7 +41,8 @@ METRIC = ("indexer q-k pairs/s + exact top-k at 1M ctx (% TC peak); "
           "replay entries/s (% HBM)")
 REPLAY_BYTES_PER_ENTRY = {  # idx 4 + key row d*esize + key scale + out 4 + q/w share
     "e4m3": 4 + 128 + 4 + 4 + 4.25, "bf16": 4 + 256 + 4 + 4.25}
-WORKLOADS = {"glm_1m": si.glm_1m, "mixed_contexts": si.mixed_contexts,
+WORKLOADS = {"glm_1m": si.glm_1m, "glm_1m_adjacent": si.glm_1m_adjacent,
+             "mixed_contexts": si.mixed_contexts,
              "tiny_exact": si.tiny_exact}
 # DRAM bytes (read + write) of one full-size filter launch, from the ncu
 # capture summarised in profiles/glm_1m_launch_list_tensorcore.txt. Must be
@@ -60,6 +61,9 @@ def parse():
     ap.add_argument("--no-twopass", action="store_true")
     ap.add_argument("--no-sharded", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-grouped", action="store_true")
+    ap.add_argument("--replay-group", type=int, default=1, choices=[1, 2],
+                    help="replay of the step: 1 = per query, 2 = adjacent pairs")
     ap.add_argument("--shards", type=int, default=4, help="key ranges of the sharded selection")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=48, help="oracle sample size (queries)")
@@ -305,6 +309,7 @@ def gpu_arm(args, world, rank, local):
                   k_scale=t["k_scale"], workspace=ws, out=(idx, sc),
                   phase_events=None if events is None else events[:nph])
         hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"],
+                  group=args.replay_group,
                   out=rs)
         if events is not None:
             events[nph].record(stream)
@@ -371,6 +376,8 @@ def gpu_arm(args, world, rank, local):
         line["twopass"] = twopass(hk, case, t, dev, idx, pairs)
     if not args.no_sharded:
         line["sharded"] = sharded(hk, case, t, dev, idx, pairs, args.shards)
+    if not args.no_grouped and world == 1:
+        line["grouped_replay"] = grouped(hk, case, t, dev, idx, ws, args, pk)
     if not args.no_backward and H in (16, 32, 64):
         line["backward"] = backward(hk, case, t, dev, idx, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -484,6 +491,71 @@ def sharded(hk, case, t, dev, idx_ref, pairs, P):
     del ws3
     return {"value": pairs / (ms / 1e3), "unit": "pairs/s", "ms": ms, "shards": P,
             "same_idx_as_hytopk": same}
+
+
+def adjacent_share(idx):
+    """Mean fraction of query 2i's selected keys that query 2i+1 also selected."""
+    a = idx.cpu().numpy()
+    m = a.shape[0] // 2
+    k = a.shape[1]
+    shared = [np.intersect1d(a[2 * i][a[2 * i] >= 0], a[2 * i + 1][a[2 * i + 1] >= 0]).size
+              for i in range(m)]
+    return float(np.mean(shared)) / k if m else 0.0
+
+
+def time_replays(hk, t, idx, group, reps=5):
+    """Median CUDA-event time of `reps` replays (after one warm-up) and the result."""
+    import torch
+
+    times = []
+    out = None
+    for rep in range(reps + 1):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        out = hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"],
+                        group=group)
+        b.record()
+        torch.cuda.synchronize()
+        if rep:
+            times.append(a.elapsed_time(b))
+    return statistics.median(times), out
+
+
+def grouped(hk, case, t, dev, idx, ws, args, pk):
+    """Replay with adjacent queries grouped in pairs (group 2: the union of the
+    two index lists is gathered once) against the per-query replay: on this
+    workload's own selection, and for the 1M-key workload also on the same
+    shapes with neighbouring queries alike (glm_1m_adjacent, whose selection is
+    run once here). Both replays must agree bit for bit."""
+    import torch
+
+    def compare(tt, ii):
+        n, k_top = ii.shape
+        ms1, r1 = time_replays(hk, tt, ii, 1)
+        ms2, r2 = time_replays(hk, tt, ii, 2)
+        same = bool(torch.equal(r1.view(torch.int32), r2.view(torch.int32)))
+        if not same:
+            raise RuntimeError("grouped replay differs from the per-query replay")
+        share = adjacent_share(ii)
+        nbytes = n * k_top * REPLAY_BYTES_PER_ENTRY[case["dtype"]]
+        return {"adjacent_share": share, "single_ms": ms1, "grouped_ms": ms2,
+                "speedup": ms1 / ms2, "grouped_entries_per_s": n * k_top / (ms2 / 1e3),
+                "grouped_frac_hbm_of_measured": nbytes / (ms2 / 1e3) / 1e9 / pk["hbm_gbs"],
+                "gathered_rows_vs_single": 1.0 - share / 2, "same_scores": same}
+
+    res = {args.workload: compare(t, idx)}
+    if args.workload == "glm_1m" and not args.queries:
+        adj = si.glm_1m_adjacent()
+        ta = si.to_torch(adj, dev)
+        n, H, d = adj["q"].shape
+        ia, _, _ = hk.select(ta["q"], ta["k"], ta["w"], ta["positions"], adj["k_top"],
+                             q_scale=ta["q_scale"], k_scale=ta["k_scale"], workspace=ws)
+        r = compare(ta, ia)
+        r["rho"] = 0.98
+        res["glm_1m_adjacent"] = r
+        del ta, ia
+    return res
 
 
 def backward(hk, case, t, dev, idx, pk):

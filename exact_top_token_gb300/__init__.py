@@ -35,7 +35,7 @@ symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", 
            "hytopk_twopass_workspace_size", "hytopk_select_twopass", "hytopk_select_noalloc",
            "hytopk_select_sharded_workspace_size", "hytopk_select_sharded",
            "hytopk_replay_backward", "hytopk_select_varlen_workspace_size",
-           "hytopk_select_varlen", "hytopk_replay_varlen",
+           "hytopk_select_varlen", "hytopk_replay_varlen", "hytopk_replay_grouped",
            "hytopk_status_string", "hytopk_version")
 
 
@@ -85,6 +85,8 @@ def load(path: str | None = None):
     lib.hytopk_select_ex.argtypes = sel + [P, P]
     lib.hytopk_replay.restype = I
     lib.hytopk_replay.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
+    lib.hytopk_replay_grouped.restype = I
+    lib.hytopk_replay_grouped.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, P, P]
     lib.hytopk_twopass_workspace_size.restype = Z
     lib.hytopk_twopass_workspace_size.argtypes = [I, I, I, I, I, I, I]
     lib.hytopk_select_twopass.restype = I
@@ -353,8 +355,11 @@ def read_stats(st) -> dict:
     return {name: getattr(s, name) for name, _ in Stats._fields_}
 
 
-def replay(q, k, w, idx, *, q_scale=None, k_scale=None, status=None, out=None, stream=None):
-    """Selection replay: scores [n,k] of the stored indices idx [n,k]."""
+def replay(q, k, w, idx, *, q_scale=None, k_scale=None, status=None, out=None, group=1,
+           stream=None):
+    """Selection replay: scores [n,k] of the stored indices idx [n,k].
+    ``group=2`` replays adjacent query pairs over the union of their indices
+    (same result)."""
     import torch
 
     lib = load()
@@ -362,8 +367,14 @@ def replay(q, k, w, idx, *, q_scale=None, k_scale=None, status=None, out=None, s
     k_top = idx.shape[1]
     _check_tensor("idx", idx, dev, torch.int32, (n, k_top))
     res = out if out is not None else torch.empty((n, k_top), dtype=torch.float32, device=dev)
-    st = lib.hytopk_replay(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(idx), n,
-                           L, H, d, k_top, dt, _ptr(res), _ptr(status), _stream(dev, stream))
+    if group == 1:
+        st = lib.hytopk_replay(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(idx),
+                               n, L, H, d, k_top, dt, _ptr(res), _ptr(status),
+                               _stream(dev, stream))
+    else:
+        st = lib.hytopk_replay_grouped(_ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w),
+                                       _ptr(idx), n, L, H, d, k_top, dt, group, _ptr(res),
+                                       _ptr(status), _stream(dev, stream))
     if st != 0:
         raise HytopkError(st, "hytopk_replay")
     return res

@@ -217,6 +217,26 @@ hytopk_status hytopk_replay(const void* q, const float* q_scale, const void* k,
   return HYTOPK_OK;
 }
 
+hytopk_status hytopk_replay_grouped(const void* q, const float* q_scale, const void* k,
+                                    const float* k_scale, const float* w, const int32_t* idx,
+                                    int n, int L, int H, int d, int k_top, hytopk_dtype dt,
+                                    int group, float* scores_out, uint32_t* dev_status,
+                                    cudaStream_t stream) {
+  if (group != 1 && group != 2) return HYTOPK_INVALID_ARG;
+  hytopk_status s = check_shape(n, L, H, d, k_top, dt);
+  if (s != HYTOPK_OK) return s;
+  s = check_inputs(q, q_scale, k, k_scale, w, dt, n);
+  if (s != HYTOPK_OK) return s;
+  if (n == 0) return HYTOPK_OK;
+  if (!idx || !scores_out) return HYTOPK_INVALID_ARG;
+  const Problem p = make_problem(q, q_scale, k, k_scale, w, nullptr, n, L, H, d, k_top, dt);
+  if (group == 2 && replay_pair_supported(p))
+    HYTOPK_TRY(launch_replay_pair(p, idx, scores_out, dev_status, stream));
+  else
+    HYTOPK_TRY(launch_replay(p, idx, scores_out, dev_status, stream));
+  return HYTOPK_OK;
+}
+
 // Two-pass workspace: the per-CTA candidate lists of the read-back kernel, the
 // halved folded weights of the queries (padded by one query block), then the
 // score-table chunk.

@@ -211,8 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
   using C_ = Cfg<D, DT, H>;
   constexpr int STAGES = C_::STAGES, CPRS = C_::CPRS;
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = tc::align1024(smem_dyn);
   uint8_t* ring = smem + C_::RING_OFF;
   uint8_t* aq = smem + C_::AQ_OFF;
   uint8_t* ak = smem + C_::AK_OFF;

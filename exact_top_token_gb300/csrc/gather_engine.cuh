@@ -16,6 +16,15 @@
 // The CTA then finishes the query together: the r-th best sample (threshold),
 // nothing (replay), or an exact top-k of the rescored row (recovery).
 //
+// Paired replay (kReplayPair) serves two adjacent queries per item. Adjacent
+// tokens select mostly the same keys (HyScale summary, "What the paper
+// found"; explainer, limits paragraph), so the item gathers the union of the
+// two stored index lists once (the first query's list, then the second
+// query's other keys, matched through a shared-memory hash table) and one MMA
+// with both queries' rows (N = 2H) scores every gathered key for both; each
+// query keeps the scores of its own entries. Scores equal the single-query
+// replay bit for bit.
+//
 //   warps 0..3  producers (cp.async gather, 128 threads)
 //   warp 4      MMA issuer; warp 5 TMEM allocator
 //   warps 8..11 epilogue
@@ -32,16 +41,29 @@ constexpr int kProducers = 128;
 constexpr int kEpiFirstWarp = 8;
 constexpr int kSlots = 2;  // TMEM accumulators
 
-enum Mode { kThreshold = 0, kReplay = 1, kRecover = 2 };
+enum Mode { kThreshold = 0, kReplay = 1, kRecover = 2, kReplayPair = 3 };
+
+// Paired replay: the hash table of the first query's keys (8 B per slot, at
+// most half full) lives in the stage ring while the rows are built, so k is
+// bounded by the ring.
+constexpr int kMaxPairTopK = 2048;
+__host__ __device__ constexpr int pair_table_slots(int k_top) {
+  int ts = 1024;
+  while (ts < 2 * k_top) ts *= 2;
+  return ts;
+}
 
 template <int D, int DT, int H, int MODE>
 struct Cfg {
   static constexpr int ES = DT == 0 ? 2 : 1;
   static constexpr int RB = D * ES;
   using Geo = tc::Geo<RB>;
-  static constexpr int NQ = H < 16 ? 16 : H;         // MMA N (query rows, zero padded)
+  static constexpr bool PAIR = MODE == kReplayPair;
+  static constexpr int QROWS = PAIR ? 2 * H : H;     // query rows of the operand
+  static constexpr int NQ = QROWS < 16 ? 16 : QROWS; // MMA N (zero padded)
   static constexpr int CPR = RB / 16;                // 16-byte chunks per row
-  static constexpr int STAGES = RB == 256 ? 3 : 4;
+  static constexpr int STAGES =
+      PAIR ? (RB == 256 ? 3 : (RB == 128 ? 4 : 8)) : (RB == 256 ? 3 : 4);
   static constexpr int KT_BYTES = 128 * RB;
   static constexpr int RING = STAGES * KT_BYTES;
   static constexpr int TMEM_COLS = (kSlots * NQ) < 32 ? 32 : (kSlots * NQ);
@@ -50,6 +72,9 @@ struct Cfg {
   static constexpr int NBARS = 2 * STAGES + 2 * kSlots;
   // host computes the union size (depends on k for recovery)
   static_assert(H >= 1 && H <= 128 && (H & (H - 1)) == 0, "H");
+  static_assert(!PAIR || (H <= 64 && RING >= pair_table_slots(kMaxPairTopK) * 8 +
+                                                 kMaxPairTopK * 4 + 8),
+                "paired replay: 2H <= 128 columns, build scratch inside the ring");
 };
 
 struct GArgs {
@@ -84,14 +109,148 @@ struct GArgs {
   uint32_t* status;
 };
 
+// Paired replay: the rows of an item are the union of the two queries'
+// entries, ordered so that whole warps serve one query where they can: first
+// the first query's entries whose key the second query also holds (rja and
+// rjb both set), then its other entries (rjb = -1), then the second query's
+// entries whose key the first query does not hold (rja = -1, key in xkey).
+// A first-query row's key is its stored index (unchecked, as in the
+// single-query replay), read again from the list. The first query's keys
+// are matched through an open-addressing table in the stage ring (linear
+// probing, at most half full); a repeated entry of the second query gets a
+// row of its own. Second-query entries outside [0, L) are written here (-inf for -1, else NaN and a
+// status bit). Whole CTA; returns the number of rows (k + second-only rows).
+static __device__ __forceinline__ uint32_t pair_hash(int s, int ts) {
+  return ((uint32_t)s * 0x9E3779B1u) >> (33 - __ffs(ts));
+}
+
+static __device__ __forceinline__ int build_pair_rows(const GArgs& a, int t, int tB,
+                                                      uint8_t* scratch, int32_t* xkey,
+                                                      int16_t* rja, int16_t* rjb, int* ucount) {
+  constexpr int KPT = (kMaxPairTopK + kThreads - 1) / kThreads;  // entries per thread
+  const int k = a.k_top;
+  const int ts = pair_table_slots(k);
+  int32_t* tkey = reinterpret_cast<int32_t*>(scratch);
+  int32_t* trow = tkey + ts;
+  int32_t* pjb = trow + ts;   // [k] second-query entry paired with first-query entry j
+  int* cnt = pjb + k;         // [2] rows taken from the front / from the back of [0, k)
+  // both index lists in registers at once (entry j = threadIdx.x + i * kThreads)
+  int sa[KPT], sb[KPT];
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const int j = (int)threadIdx.x + i * kThreads;
+    sa[i] = j < k ? __ldg(a.idx + (size_t)t * k + j) : -1;
+    sb[i] = (j < k && tB >= 0) ? __ldg(a.idx + (size_t)tB * k + j) : -1;
+  }
+  for (int i = threadIdx.x; i < ts; i += kThreads) tkey[i] = -1;
+  for (int j = threadIdx.x; j < k; j += kThreads) pjb[j] = -1;
+  if (threadIdx.x == 0) {
+    *ucount = 0;
+    cnt[0] = cnt[1] = 0;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const unsigned lanes_below = (1u << lane) - 1u;
+  if (tB >= 0) {
+    // the first query's keys -> one of its entries that holds the key
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const int j = (int)threadIdx.x + i * kThreads;
+      const int s = sa[i];
+      if (j >= k || s < 0 || s >= a.L) continue;
+      uint32_t h = pair_hash(s, ts);
+      for (int probe = 0; probe < ts; ++probe) {  // ends: at most k keys in 2k slots or more
+        const int prev = tc::atom_cas_shared(tkey + h, -1, s);
+        if (prev == -1) {
+          trow[h] = j;
+          break;
+        }
+        if (prev == s) break;
+        h = (h + 1) & (uint32_t)(ts - 1);
+      }
+    }
+    __syncthreads();
+    // the second query's entries: paired with a first-query entry, or rows of their own
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+      const int j = (int)threadIdx.x + i * kThreads;
+      const int s = sb[i];
+      bool own = false;
+      if (j < k) {
+        if (s < 0 || s >= a.L) {
+          float v = -__int_as_float(0x7f800000);
+          if (s != -1) {
+            v = __int_as_float(0x7fc00000);
+            if (a.status) atomicOr(a.status, HYTOPK_DEV_REPLAY_BAD_INDEX);
+          }
+          a.out[(size_t)tB * k + j] = v;
+        } else {
+          int row = -1;
+          uint32_t h = pair_hash(s, ts);
+          for (int probe = 0; probe < ts; ++probe) {
+            const int key = tkey[h];
+            if (key == s) {
+              row = trow[h];
+              break;
+            }
+            if (key == -1) break;
+            h = (h + 1) & (uint32_t)(ts - 1);
+          }
+          own = row < 0 || tc::atom_cas_shared(pjb + row, -1, j) != -1;
+        }
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, own);
+      if (m) {
+        int u0 = 0;
+        if (lane == 0) u0 = tc::atom_add_shared(ucount, __popc(m));
+        u0 = __shfl_sync(0xffffffffu, u0, 0);
+        if (own) {
+          const int u = u0 + __popc(m & lanes_below);
+          xkey[u] = s;
+          rja[k + u] = -1;
+          rjb[k + u] = (int16_t)j;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // the first query's entries: paired ones from the front, the others from the back
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const int j = (int)threadIdx.x + i * kThreads;
+    const bool in = j < k;
+    const int jb = in ? pjb[j] : -1;
+    const bool front = in && jb >= 0;
+    const unsigned mf = __ballot_sync(0xffffffffu, front);
+    const unsigned mb = __ballot_sync(0xffffffffu, in && !front);
+    int f0 = 0, b0 = 0;
+    if (lane == 0) {
+      if (mf) f0 = tc::atom_add_shared(cnt, __popc(mf));
+      if (mb) b0 = tc::atom_add_shared(cnt + 1, __popc(mb));
+    }
+    f0 = __shfl_sync(0xffffffffu, f0, 0);
+    b0 = __shfl_sync(0xffffffffu, b0, 0);
+    if (in) {
+      const int r = front ? f0 + __popc(mf & lanes_below) : k - 1 - (b0 + __popc(mb & lanes_below));
+      rja[r] = (int16_t)j;
+      rjb[r] = (int16_t)jb;
+    }
+  }
+  __syncthreads();
+  const int n_rows = k + *ucount;
+  __syncthreads();  // the table (in the stage ring) is free again after this
+  return n_rows;
+}
+
 template <int D, int DT, int H, int MODE>
 __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   using C_ = Cfg<D, DT, H, MODE>;
   using Geo = typename C_::Geo;
   constexpr int NQ = C_::NQ, STAGES = C_::STAGES, CPR = C_::CPR, RB = C_::RB;
+  constexpr bool PAIR = C_::PAIR;
+  constexpr bool REPLAY = MODE == kReplay || PAIR;
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = tc::align1024(smem_dyn);
   uint8_t* qbuf = smem + C_::Q_OFF;
   uint8_t* ring = smem + C_::U_OFF;
   uint8_t* tail = ring + a.u_bytes;
@@ -104,10 +263,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   uint32_t* tmem_slot = misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   int* item_sh = reinterpret_cast<int*>(misc + 2);
+  int* ucount = reinterpret_cast<int*>(misc + 3);                // paired: union size
   float* wq_s = reinterpret_cast<float*>(misc + 4);              // [H]
   uint32_t* keys_s = reinterpret_cast<uint32_t*>(wq_s + 128);    // [kMaxSamples] (threshold)
   RadixScratch& rsc = *reinterpret_cast<RadixScratch*>(ring);    // after the pipeline drains
   uint64_t* sel = reinterpret_cast<uint64_t*>(ring + sizeof(RadixScratch));
+  // paired replay, after the ring: the keys of the second query's own rows,
+  // then per row the entry of each query it serves (-1: none)
+  int32_t* xkey = reinterpret_cast<int32_t*>(ring + C_::RING);  // [k]
+  int16_t* rja = reinterpret_cast<int16_t*>(xkey + a.k_top);      // [2k]
+  int16_t* rjb = rja + 2 * a.k_top;                               // [2k]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -135,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   int p_stage = 0, m_stage = 0, m_slot = 0, e_slot = 0;
   uint32_t p_phase = 0, m_phase = 0, m_aphase = 0, e_aphase = 0;
 
-  const int n_items = MODE == kThreshold ? a.n_pad : (MODE == kReplay ? a.n : 0);
+  const int n_items =
+      MODE == kThreshold ? a.n_pad : (MODE == kReplay ? a.n : (PAIR ? (a.n + 1) / 2 : 0));
   const uint32_t n_failed = MODE == kRecover ? a.counters[kCtrFailed] : 0u;
   const bool fallback = n_failed > HYTOPK_MAX_RECOVERY_ROWS;
   const int n_rec = MODE == kRecover ? (fallback ? a.n_pad : (int)n_failed) : 0;
@@ -155,10 +321,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
     }
     if (*abort_flag) break;
     int slot = -1, t = -1, ctx = 0, nrows = 0, M = 0, r = 0;
+    int tB = -1;  // paired replay: the second query (t is the first)
     SampleStep step{};
     if (MODE == kReplay) {
       t = item;
       nrows = a.k_top;
+    } else if (PAIR) {
+      t = 2 * item;
+      tB = t + 1 < a.n ? t + 1 : -1;
     } else {
       slot = MODE == kThreshold ? item : (fallback ? item : a.failed_list[item]);
       t = a.perm[slot];
@@ -178,12 +348,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
         nrows = ctx;
       }
     }
-    const int ntiles = (nrows + kTileKeys - 1) / kTileKeys;
-    // key of row j of this query's list (replay: the stored index, unchecked)
+    // key of row j of this query's list (replay: the stored index, unchecked;
+    // paired replay: the union row, always inside [0, L))
     auto key_of = [&](int j) -> int {
       if (j >= nrows) return -1;
       if (MODE == kThreshold) return step.at(j);
       if (MODE == kReplay) return __ldg(a.idx + (size_t)t * a.k_top + j);
+      if (PAIR)
+        return j < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + rja[j]) : xkey[j - a.k_top];
       return j;
     };
 
@@ -191,15 +363,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
     {
       // e4m3 queries against bf16 keys (replay only; the other modes read the
       // packed operand): D-byte rows, 8 codes per 16-byte chunk of the operand
-      const bool q8 = DT == 0 && MODE == kReplay && a.q_e4m3;
+      const bool q8 = DT == 0 && REPLAY && a.q_e4m3;
       const int q_row_bytes = q8 ? D : RB;
+      // paired replay: rows H..2H-1 are the second query's (zero if there is none)
       const uint8_t* qsrc =
-          MODE == kReplay ? reinterpret_cast<const uint8_t*>(a.q) + (size_t)t * H * q_row_bytes
-                          : reinterpret_cast<const uint8_t*>(a.qp) + (size_t)slot * H * RB;
+          REPLAY ? reinterpret_cast<const uint8_t*>(a.q) + (size_t)t * H * q_row_bytes
+                 : reinterpret_cast<const uint8_t*>(a.qp) + (size_t)slot * H * RB;
+      const int q_rows = PAIR ? (tB >= 0 ? 2 * H : H) : H;
       for (int f = threadIdx.x; f < NQ * CPR; f += kThreads) {
         const int row = f / CPR, c = f % CPR;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < H) {
+        if (row < q_rows) {
           if (q8)
             v = e4m3x8_to_bf16(
                 *reinterpret_cast<const uint2*>(qsrc + (size_t)row * q_row_bytes + c * 8));
@@ -208,12 +382,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
         }
         *reinterpret_cast<uint4*>(qbuf + Geo::chunk_offset(row, c, NQ)) = v;
       }
-      for (int h = threadIdx.x; h < H; h += kThreads) {
-        float hw;  // halved folded weight, as in the prep kernel
-        if (MODE == kReplay) {
-          float wv = a.w[(size_t)t * H + h];
-          if (DT == 1 || a.q_e4m3) wv *= a.q_scale[(size_t)t * H + h];
-          hw = 0.5f * wv;
+      for (int h = threadIdx.x; h < C_::QROWS; h += kThreads) {
+        float hw = 0.0f;  // halved folded weight, as in the prep kernel
+        if (REPLAY) {
+          // row h of the operand: head h of t, or head h - H of the second query
+          if (h < q_rows) {
+            float wv = a.w[(size_t)t * H + h];
+            if (DT == 1 || a.q_e4m3) wv *= a.q_scale[(size_t)t * H + h];
+            hw = 0.5f * wv;
+          }
         } else {
           hw = a.wq[(size_t)slot * H + h];
         }
@@ -222,6 +399,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       tc::fence_proxy_async_smem();
       __syncthreads();
     }
+    if constexpr (PAIR) nrows = build_pair_rows(a, t, tB, ring, xkey, rja, rjb, ucount);
+    const int ntiles = (nrows + kTileKeys - 1) / kTileKeys;
 
     if (warp < 4) {
       // ---------------- producers: gather 128 key rows per tile ----------------
@@ -326,8 +505,81 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
         const bool valid = s >= 0 && s < a.L;
         stream::HeadSum<H> hs;
         hs.reset();
-        float sc;
-        if (H >= 32) {
+        float sc = 0.0f, scB = 0.0f;
+        int ja = -1, jb = -1;  // paired replay: the entries this row serves
+        if constexpr (PAIR) {
+          // columns 0..H-1: the first query's heads, H..2H-1: the second's, with
+          // the per-head arithmetic and order of the single-query replay; a warp
+          // none of whose rows serves a query skips that query's columns
+          if (j < nrows) {
+            ja = rja[j];
+            jb = rjb[j];
+          }
+          const bool need_a = __any_sync(0xffffffffu, ja >= 0);
+          const bool need_b = __any_sync(0xffffffffu, jb >= 0);
+          stream::HeadSum<H> hb;
+          hb.reset();
+          if constexpr (NQ >= 64) {
+            if (need_a) {
+#pragma unroll
+              for (int c0 = 0; c0 < H; c0 += 32) {
+                float v[32];
+                tc::tmem_ld32(taddr + c0, v);
+                tc::tmem_wait_ld(v);
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                  const float4 w4 = *reinterpret_cast<const float4*>(wq_s + c0 + h);
+                  hs.add_pair(c0 + h, v[h], v[h + 1], w4.x, w4.y);
+                  hs.add_pair(c0 + h + 2, v[h + 2], v[h + 3], w4.z, w4.w);
+                }
+              }
+              sc = hs.total();
+            }
+            if (need_b) {
+#pragma unroll
+              for (int c0 = 0; c0 < H; c0 += 32) {
+                float v[32];
+                tc::tmem_ld32(taddr + H + c0, v);
+                tc::tmem_wait_ld(v);
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                  const float4 w4 = *reinterpret_cast<const float4*>(wq_s + H + c0 + h);
+                  hb.add_pair(c0 + h, v[h], v[h + 1], w4.x, w4.y);
+                  hb.add_pair(c0 + h + 2, v[h + 2], v[h + 3], w4.z, w4.w);
+                }
+              }
+              scB = hb.total();
+            }
+          } else if constexpr (NQ == 32) {  // H = 16: one load holds both queries
+            float v[32];
+            tc::tmem_ld32(taddr, v);
+            tc::tmem_wait_ld(v);
+#pragma unroll
+            for (int h = 0; h < 16; h += 2) {
+              hs.add_pair(h, v[h], v[h + 1], wq_s[h], wq_s[h + 1]);
+              hb.add_pair(h, v[16 + h], v[17 + h], wq_s[16 + h], wq_s[17 + h]);
+            }
+            sc = hs.total();
+            scB = hb.total();
+          } else {  // H <= 8
+            float v[16];
+            tc::tmem_ld16(taddr, v);
+            tc::tmem_wait_ld(v);
+            if (H == 1) {
+              sc = stream::single_head_score<H>(v[0], wq_s[0]);
+              scB = stream::single_head_score<H>(v[1], wq_s[1]);
+            } else {
+#pragma unroll
+              for (int h = 0; h < (H < 8 ? H : 8); h += 2) {
+                hs.add_pair(h, v[h], v[h + 1], wq_s[h], wq_s[h + 1]);
+                hb.add_pair(h, v[H + h], v[H + h + 1], wq_s[H + h], wq_s[H + h + 1]);
+              }
+              sc = hs.total();
+              scB = hb.total();
+            }
+          }
+          scB = finish_score(scB, ks);
+        } else if (H >= 32) {
 #pragma unroll
           for (int c0 = 0; c0 < H; c0 += 32) {
             float v[32];
@@ -365,7 +617,21 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
         if (j < nrows) {
           if (MODE == kThreshold) {
             keys_s[j] = desc32(sc);
-          } else if (MODE == kReplay) {
+          } else if (PAIR) {
+            if (ja >= 0) {
+              float v = sc;
+              if (!valid) {
+                if (s == -1) {
+                  v = -__int_as_float(0x7f800000);
+                } else {
+                  v = __int_as_float(0x7fc00000);
+                  if (a.status) atomicOr(a.status, HYTOPK_DEV_REPLAY_BAD_INDEX);
+                }
+              }
+              a.out[(size_t)t * a.k_top + ja] = v;
+            }
+            if (jb >= 0) a.out[(size_t)tB * a.k_top + jb] = scB;
+          } else if (REPLAY) {
             float v = sc;
             if (!valid) {
               if (s == -1) {
@@ -414,10 +680,54 @@ inline int gather_smem_bytes(int k_top, int* u_bytes) {
   if (MODE == kThreshold) post = (int)sizeof(RadixScratch);
   if (MODE == kRecover) post = (int)sizeof(RadixScratch) + sort_capacity(k_top) * 8;
   int u = C_::RING > post ? C_::RING : post;
+  if (MODE == kReplayPair) u = C_::RING + 3 * k_top * 4;  // + xkey, rja, rjb
   u = (u + 15) / 16 * 16;
   *u_bytes = u;
   const int tail = 8 * C_::NBARS + 16 + 128 * 4 + (MODE == kThreshold ? kMaxSamples * 4 : 0);
   return 1024 + C_::U_OFF + u + tail;
+}
+
+// Host launch of one instantiation (dynamic shared memory set per call).
+template <int D, int DT, int H, int MODE>
+cudaError_t gather_go(const GArgs& a0, int grid, cudaStream_t st) {
+  GArgs a = a0;
+  int u = 0;
+  const int smem = gather_smem_bytes<D, DT, H, MODE>(a.k_top, &u);
+  a.u_bytes = u;
+  auto fn = k_gather<D, DT, H, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  fn<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, int DT, int H>
+cudaError_t gather_modes(int mode, const GArgs& a, int grid, cudaStream_t st) {
+  switch (mode) {
+    case kThreshold: return gather_go<D, DT, H, kThreshold>(a, grid, st);
+    case kReplay: return gather_go<D, DT, H, kReplay>(a, grid, st);
+    case kRecover: return gather_go<D, DT, H, kRecover>(a, grid, st);
+    case kReplayPair:
+      if constexpr (H <= 64) return gather_go<D, DT, H, kReplayPair>(a, grid, st);
+      break;
+  }
+  return cudaErrorInvalidValue;
+}
+
+// Every mode for the H values of the C ABI (powers of two up to 128).
+template <int D, int DT>
+cudaError_t gather_launch(int H, int mode, const GArgs& a, int grid, cudaStream_t st) {
+  switch (H) {
+    case 1: return gather_modes<D, DT, 1>(mode, a, grid, st);
+    case 2: return gather_modes<D, DT, 2>(mode, a, grid, st);
+    case 4: return gather_modes<D, DT, 4>(mode, a, grid, st);
+    case 8: return gather_modes<D, DT, 8>(mode, a, grid, st);
+    case 16: return gather_modes<D, DT, 16>(mode, a, grid, st);
+    case 32: return gather_modes<D, DT, 32>(mode, a, grid, st);
+    case 64: return gather_modes<D, DT, 64>(mode, a, grid, st);
+    case 128: return gather_modes<D, DT, 128>(mode, a, grid, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace gather

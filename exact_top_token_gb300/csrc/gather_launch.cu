@@ -1,5 +1,6 @@
 // gather_launch.cu -- host launchers of the gather engine: the sampled
-// threshold and recovery phases of hytopk_select, and hytopk_replay.
+// threshold and recovery phases of hytopk_select, hytopk_replay and the paired
+// replay of hytopk_replay_grouped.
 #include "gather_engine.cuh"
 #include "launch.h"
 
@@ -92,6 +93,23 @@ cudaError_t launch_replay(const Problem& p, const int32_t* idx, float* out, uint
   a.out = out;
   a.status = status;
   return dispatch(p, gather::kReplay, a, capped_grid(p.n), st);
+}
+
+bool replay_pair_supported(const Problem& p) {
+  return p.H <= 64 && p.k_top <= gather::kMaxPairTopK;
+}
+
+cudaError_t launch_replay_pair(const Problem& p, const int32_t* idx, float* out, uint32_t* status,
+                               cudaStream_t st) {
+  gather::GArgs a = base_args(p);
+  a.q = p.q;
+  a.q_scale = p.q_scale;
+  a.q_e4m3 = p.qdt == 1 && p.dt == 0;
+  a.w = p.w;
+  a.idx = idx;
+  a.out = out;
+  a.status = status;
+  return dispatch(p, gather::kReplayPair, a, capped_grid((p.n + 1) / 2), st);
 }
 
 }  // namespace hytopk

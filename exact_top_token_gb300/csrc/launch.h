@@ -23,6 +23,10 @@ cudaError_t launch_recover(const Problem& p, const SelectWs& ws, int32_t* idx_ou
                            float* scores_out, cudaStream_t st);
 cudaError_t launch_replay(const Problem& p, const int32_t* idx, float* out, uint32_t* status,
                           cudaStream_t st);
+// adjacent queries 2i, 2i+1 replayed together over the union of their indices
+bool replay_pair_supported(const Problem& p);
+cudaError_t launch_replay_pair(const Problem& p, const int32_t* idx, float* out, uint32_t* status,
+                               cudaStream_t st);
 cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, const float* hw,
                          uint32_t* status, cudaStream_t st);
 

@@ -325,8 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Geo = typename C_::Geo;
   constexpr int G = C_::G, NG = C_::NG, QB = C_::QB, STAGES = C_::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) &
-                                             ~uintptr_t(1023));
+  uint8_t* smem = tc::align1024(smem_dyn);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::BAR_OFF);
   uint64_t* k_full = bars;
   uint64_t* k_empty = bars + STAGES;

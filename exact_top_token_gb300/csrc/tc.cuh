@@ -26,6 +26,29 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte boundary of the dynamic shared memory, taken as an
+// offset from the array itself: pointers derived from it keep the shared
+// address space (an integer round trip would leave them generic).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* base) {
+  return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
+// Shared-memory atomics by shared address (atom.shared, whatever the
+// compiler can prove about the pointer).
+__device__ __forceinline__ int atom_cas_shared(int* p, int cmp, int val) {
+  int old;
+  asm volatile("atom.shared.cas.b32 %0, [%1], %2, %3;"
+               : "=r"(old)
+               : "r"(smem_u32(p)), "r"(cmp), "r"(val)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ int atom_add_shared(int* p, int v) {
+  int old;
+  asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

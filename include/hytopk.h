@@ -194,6 +194,21 @@ HYTOPK_API hytopk_status hytopk_replay(const void* q, const float* q_scale, cons
                             int L, int H, int d, int k_top, hytopk_dtype dt, float* scores_out,
                             uint32_t* dev_status, cudaStream_t stream);
 
+/* Replay with adjacent queries grouped (HyScale summary, "What the paper
+ * found", and Explainer, limits paragraph: neighbouring tokens select mostly
+ * the same keys). group = 1 is hytopk_replay. group = 2 replays queries 2i
+ * and 2i+1 together: the union of their two index lists is gathered once and
+ * scored for both, so a key both select is read once. Results, -inf / NaN
+ * entries and status bits are those of hytopk_replay, bit for bit. Grouping
+ * applies when H <= 64 and k_top <= 2048; other shapes run hytopk_replay.
+ * Any other group returns HYTOPK_INVALID_ARG. */
+HYTOPK_API hytopk_status hytopk_replay_grouped(const void* q, const float* q_scale, const void* k,
+                                               const float* k_scale, const float* w,
+                                               const int32_t* idx, int n, int L, int H, int d,
+                                               int k_top, hytopk_dtype dt, int group,
+                                               float* scores_out, uint32_t* dev_status,
+                                               cudaStream_t stream);
+
 /* Gradients of the indexer score at the selected entries, with the replay
  * rescoring fused in (Explainer, key-observation paragraph: the indexer's own
  * loss reads only the scores at those entries; selection-replay paragraph:

@@ -87,10 +87,13 @@ def spaced_positions(L: int, n: int) -> np.ndarray:
 
 
 def random_case(L, n, H, d, k_top, dtype="bf16", seed=0, positions="last", kind="normal",
-                name=None):
+                name=None, pair_rho=None):
     """A general case. kind="normal": q,k ~ N(0,1)/sqrt(d), w ~ N(0,1)/sqrt(H);
     kind="int": q,k integers in [-3,3], w integers in {1,2} (scores exact in fp32).
-    positions: "last", "spaced", "random" or an int32 array."""
+    positions: "last", "spaced", "random" or an int32 array.
+    pair_rho (normal data): query 2i+1 becomes rho * query 2i + sqrt(1 - rho^2)
+    * its own draw, with the weights of query 2i, so that neighbouring queries
+    select mostly the same keys, as adjacent tokens do."""
     g = rng_for(seed)
     if kind == "normal":
         qf = g.standard_normal((n, H, d), dtype=np.float32) / np.float32(np.sqrt(d))
@@ -102,6 +105,11 @@ def random_case(L, n, H, d, k_top, dtype="bf16", seed=0, positions="last", kind=
         w = g.integers(1, 3, size=(n, H)).astype(np.float32)
     else:
         raise ValueError(kind)
+    if pair_rho is not None:
+        m = n // 2
+        rho = np.float32(pair_rho)
+        qf[1:2 * m:2] = rho * qf[0:2 * m:2] + np.float32(np.sqrt(1.0 - pair_rho ** 2)) * qf[1:2 * m:2]
+        w[1:2 * m:2] = w[0:2 * m:2]
     if isinstance(positions, str):
         if positions == "last":
             pos = last_positions(L, n)
@@ -136,6 +144,14 @@ def glm_1m(seed: int = 2, L=1 << 20, n=8192, H=64, d=128, k_top=2048):
     """The GLM-5.1-like one-GPU slice at 1M keys: n last queries, fp8 e4m3 with
     per-token (key) and per-token-head (query) fp32 scales."""
     return random_case(L, n, H, d, k_top, "e4m3", seed, "last", "normal", name="glm_1m")
+
+
+def glm_1m_adjacent(seed: int = 2, rho: float = 0.98, L=1 << 20, n=8192, H=64, d=128,
+                    k_top=2048):
+    """glm_1m with neighbouring queries alike (pair_rho = rho): the workload of
+    the grouped replay, where queries 2i and 2i+1 share most selected keys."""
+    return random_case(L, n, H, d, k_top, "e4m3", seed, "last", "normal",
+                       name="glm_1m_adjacent", pair_rho=rho)
 
 
 def recovery_stress(sampler, seed: int = 3, L=262144, n=2048, H=16, d=64, k_top=2048,

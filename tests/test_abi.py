@@ -198,3 +198,22 @@ def test_varlen_host_checks(lib):
     assert replay(ck=arr(0, 1000, 900, 5000)) == 1
     assert replay(idx=None) == 1 and replay(sc=None) == 1
     assert replay(cq=arr(0, 0, 0, 0), ck=arr(0, 1, 2, 3)) == 0  # no query: nothing to do
+
+
+def test_replay_grouped_host_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def call(**kw):
+        a = dict(q=fake, qs=None, k=fake, ks=None, w=fake, idx=fake, n=4, L=100, H=4, d=64,
+                 k_top=8, dt=0, g=2, sc=fake, st=None)
+        a.update(kw)
+        return lib.hytopk_replay_grouped(a["q"], a["qs"], a["k"], a["ks"], a["w"], a["idx"],
+                                         a["n"], a["L"], a["H"], a["d"], a["k_top"], a["dt"],
+                                         a["g"], a["sc"], a["st"], None)
+
+    assert call(g=0) == 1 and call(g=3) == 1
+    assert call(idx=None) == 1 and call(sc=None) == 1
+    assert call(H=3) == 2 and call(d=48) == 2
+    assert call(k=P((1 << 20) + 8)) == 5
+    assert call(n=0, idx=None) == 0  # nothing to do
