@@ -116,9 +116,9 @@ struct GArgs {
 // entries whose key the first query does not hold (rja = -1, key in xkey).
 // A first-query row's key is its stored index (unchecked, as in the
 // single-query replay), read again from the list. The first query's keys
-// are matched through an open-addressing table in the stage ring (linear
-// probing, at most half full); a repeated entry of the second query gets a
-// row of its own. Second-query entries outside [0, L) are written here (-inf for -1, else NaN and a
+// are matched through an open-addressing table in the stage ring (buckets of
+// four slots read with one 16-byte load, linear probing over buckets, at most
+// half full); a repeated entry of the second query gets a row of its own. Second-query entries outside [0, L) are written here (-inf for -1, else NaN and a
 // status bit). Whole CTA; returns the number of rows (k + second-only rows).
 static __device__ __forceinline__ uint32_t pair_hash(int s, int ts) {
   return ((uint32_t)s * 0x9E3779B1u) >> (33 - __ffs(ts));
@@ -130,6 +130,7 @@ static __device__ __forceinline__ int build_pair_rows(const GArgs& a, int t, int
   constexpr int KPT = (kMaxPairTopK + kThreads - 1) / kThreads;  // entries per thread
   const int k = a.k_top;
   const int ts = pair_table_slots(k);
+  const uint32_t nb = (uint32_t)ts / 4;  // buckets of 4 slots
   int32_t* tkey = reinterpret_cast<int32_t*>(scratch);
   int32_t* trow = tkey + ts;
   int32_t* pjb = trow + ts;   // [k] second-query entry paired with first-query entry j
@@ -158,15 +159,24 @@ static __device__ __forceinline__ int build_pair_rows(const GArgs& a, int t, int
       const int j = (int)threadIdx.x + i * kThreads;
       const int s = sa[i];
       if (j >= k || s < 0 || s >= a.L) continue;
-      uint32_t h = pair_hash(s, ts);
-      for (int probe = 0; probe < ts; ++probe) {  // ends: at most k keys in 2k slots or more
-        const int prev = tc::atom_cas_shared(tkey + h, -1, s);
+      // the first bucket (from the key's own) with a free slot; a slot lost to
+      // another key sends the thread back to the same bucket. Ends: at most k
+      // keys in 2k slots or more, and every failed claim fills a slot.
+      uint32_t b = pair_hash(s, (int)nb);
+      for (int round = 0; round < 2 * ts; ++round) {
+        const int4 v = *reinterpret_cast<const int4*>(tkey + 4 * b);
+        if (v.x == s || v.y == s || v.z == s || v.w == s) break;  // held by another entry
+        const int e = v.x == -1 ? 0 : (v.y == -1 ? 1 : (v.z == -1 ? 2 : (v.w == -1 ? 3 : 4)));
+        if (e == 4) {
+          b = (b + 1) & (nb - 1);
+          continue;
+        }
+        const int prev = tc::atom_cas_shared(tkey + 4 * b + e, -1, s);
         if (prev == -1) {
-          trow[h] = j;
+          trow[4 * b + e] = j;
           break;
         }
         if (prev == s) break;
-        h = (h + 1) & (uint32_t)(ts - 1);
       }
     }
     __syncthreads();
@@ -185,16 +195,18 @@ static __device__ __forceinline__ int build_pair_rows(const GArgs& a, int t, int
           }
           a.out[(size_t)tB * k + j] = v;
         } else {
+          // buckets from the key's own until the key or a free slot (absent)
           int row = -1;
-          uint32_t h = pair_hash(s, ts);
-          for (int probe = 0; probe < ts; ++probe) {
-            const int key = tkey[h];
-            if (key == s) {
-              row = trow[h];
+          uint32_t b = pair_hash(s, (int)nb);
+          for (uint32_t round = 0; round < nb; ++round) {
+            const int4 v = *reinterpret_cast<const int4*>(tkey + 4 * b);
+            const int e = v.x == s ? 0 : (v.y == s ? 1 : (v.z == s ? 2 : (v.w == s ? 3 : 4)));
+            if (e < 4) {
+              row = trow[4 * b + e];
               break;
             }
-            if (key == -1) break;
-            h = (h + 1) & (uint32_t)(ts - 1);
+            if (v.x == -1 || v.y == -1 || v.z == -1 || v.w == -1) break;
+            b = (b + 1) & (nb - 1);
           }
           own = row < 0 || tc::atom_cas_shared(pjb + row, -1, j) != -1;
         }
