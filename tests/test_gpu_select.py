@@ -316,3 +316,28 @@ def test_mixed_q_e4m3_k_bf16_paths_agree(hk, dev):
     i3, s3, _ = hk.select_sharded(t["q"], t["k"], t["w"], t["positions"], 300, 3,
                                   q_scale=t["q_scale"])
     assert np.array_equal(i3.cpu().numpy(), gi) and np.array_equal(s3.cpu().numpy(), gs)
+
+
+# ---- the largest k the library takes ------------------------------------------------------
+
+@pytest.mark.parametrize("dt,kind", [("bf16", "int"), ("e4m3", "normal")])
+def test_maximum_k(hk, dev, dt, kind):
+    """k = 16384 (the largest supported): queries with more and with fewer keys
+    than k; the selection against the oracle (exact on integer data), replay
+    and the two-pass path bit for bit."""
+    k_top = 16384
+    L, n = 40000, 12
+    pos = np.array([100, 16383, 16384, 16385, 20000, 25000, 30000, 33333, 36000, 38000,
+                    39000, 39999], np.int32)
+    case = si.random_case(L, n, 16, 64, k_top, dt, seed=44, positions=pos, kind=kind)
+    idx, sc, st, t = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(n), gi, gs, exact=(kind == "int"))
+    assert hk.read_stats(st)["device_status"] == 0
+    rs = hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"])
+    r = rs.cpu().numpy()
+    keep = gi >= 0
+    assert np.array_equal(r[keep], gs[keep]) and np.isneginf(r[~keep]).all()
+    i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], k_top,
+                               q_scale=t["q_scale"], k_scale=t["k_scale"])
+    assert np.array_equal(i2.cpu().numpy(), gi) and np.array_equal(s2.cpu().numpy(), gs)
