@@ -23,26 +23,40 @@ __device__ __forceinline__ int clean_position(const int32_t* positions, int t, i
 }
 
 // slot(t) = #{u : pos(u) > pos(t) or (pos(u) == pos(t) and u < t)}: a stable
-// descending sort by rank counting.
-__global__ void __launch_bounds__(1024) k_rank_by_position(const int32_t* __restrict__ positions,
-                                                            int n, int L,
-                                                            int32_t* __restrict__ perm) {
-  __shared__ int tile[1024];
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  const int mine = t < n ? clean_position(positions, t, L) : INT_MIN;
-  int rank = 0;
-  for (int base = 0; base < n; base += 1024) {
-    const int u = base + threadIdx.x;
-    tile[threadIdx.x] = u < n ? clean_position(positions, u, L) : INT_MIN;
+// descending sort by rank counting. A block of 8 warps ranks 32 queries
+// (4 per warp); the positions pass through shared memory 1024 at a time and
+// the lanes of a warp split each tile, so the grid covers every SM.
+constexpr int kRankWarps = 8, kRankPerWarp = 4, kRankTile = 1024;
+
+__global__ void __launch_bounds__(kRankWarps * 32) k_rank_by_position(
+    const int32_t* __restrict__ positions, int n, int L, int32_t* __restrict__ perm) {
+  __shared__ int tile[kRankTile];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = (blockIdx.x * kRankWarps + warp) * kRankPerWarp;
+  int mine[kRankPerWarp], rank[kRankPerWarp];
+#pragma unroll
+  for (int q = 0; q < kRankPerWarp; ++q) {
+    mine[q] = t0 + q < n ? clean_position(positions, t0 + q, L) : INT_MIN;
+    rank[q] = 0;
+  }
+  for (int base = 0; base < n; base += kRankTile) {
+    for (int i = threadIdx.x; i < kRankTile; i += blockDim.x)
+      tile[i] = base + i < n ? clean_position(positions, base + i, L) : INT_MIN;
     __syncthreads();
-    const int lim = min(1024, n - base);
-    for (int j = 0; j < lim; ++j) {
-      const int pu = tile[j];
-      rank += (pu > mine) | ((pu == mine) & (base + j < t));
+    const int lim = min(kRankTile, n - base);
+    for (int j = lane; j < lim; j += 32) {
+      const int pu = tile[j], u = base + j;
+#pragma unroll
+      for (int q = 0; q < kRankPerWarp; ++q)
+        rank[q] += (pu > mine[q]) | ((pu == mine[q]) & (u < t0 + q));
     }
     __syncthreads();
   }
-  if (t < n) perm[rank] = t;
+#pragma unroll
+  for (int q = 0; q < kRankPerWarp; ++q) {
+    const int r = __reduce_add_sync(0xffffffffu, rank[q]);
+    if (lane == 0 && t0 + q < n) perm[r] = t0 + q;
+  }
 }
 
 // Slot row of the packed query operand, in the key element type: a copy, or
@@ -135,7 +149,10 @@ cudaError_t launch_fold_weights(const Problem& p, int rows, float* hw, cudaStrea
 }
 
 cudaError_t launch_prep(const Problem& p, const SelectWs& ws, cudaStream_t st) {
-  if (p.n > 0) k_rank_by_position<<<(p.n + 1023) / 1024, 1024, 0, st>>>(p.positions, p.n, p.L, ws.perm);
+  constexpr int per_block = kRankWarps * kRankPerWarp;
+  if (p.n > 0)
+    k_rank_by_position<<<(p.n + per_block - 1) / per_block, kRankWarps * 32, 0, st>>>(
+        p.positions, p.n, p.L, ws.perm);
   if (ws.n_pad > 0) k_pack_queries<<<ws.n_pad, 128, 0, st>>>(p, ws);
   if (p.dt == 1) k_check_key_scales<<<64, 256, 0, st>>>(p.k_scale, p.L, ws.counters);
   return cudaGetLastError();
