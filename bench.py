@@ -247,12 +247,32 @@ def reference_arm(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+L2_BYTES = 129 * 2**20       # GB300 L2
+FLUSH_BYTES = 512 * 2**20    # written between timed steps when a step's data could stay in L2
+
+
+def step_bytes(case):
+    """Bytes one step touches at least: keys, queries and ~3k candidates (8 B) per query."""
+    n, H, d = case["q"].shape
+    return (case["k"].nbytes + case["q"].nbytes + n * 3 * case["k_top"] * 8)
+
+
+def needs_flush(case):
+    return step_bytes(case) < 2 * L2_BYTES
+
+
 def workload_config(case, world=1):
     n, H, d = case["q"].shape
+    mib = step_bytes(case) / 2**20
+    l2 = (f"inputs larger than L2: keys {case['k'].nbytes / 2**20:.0f} MiB + queries "
+          f"{case['q'].nbytes / 2**20:.0f} MiB + candidates, {mib:.0f} MiB per step"
+          if not needs_flush(case) else
+          f"L2 flushed before every timed step ({FLUSH_BYTES // 2**20} MiB write, not timed): "
+          f"{mib:.0f} MiB per step would fit in the {L2_BYTES // 2**20} MiB L2")
     cfg = {"workload": case["name"], "L": int(case["k"].shape[0]), "n": int(n), "H": int(H),
            "d": int(d), "k_top": int(case["k_top"]), "capacity": 8 * int(case["k_top"]),
            "positions": "last n" if case["name"] == "glm_1m" else "see synthetic_inputs",
-           "l2": "inputs larger than L2 (K 128 MiB + Q 64 MiB + 1 GiB candidate buffer per step)"}
+           "l2": l2}
     if world > 1:
         cfg["parallelism"] = (f"dp{world}: query shards of n per GPU (rank r: the r-th block of n "
                               "positions from the end), keys replicated, no collective")
@@ -322,16 +342,24 @@ def gpu_arm(args, world, rank, local):
         clocks.start()
     barrier(world)
     torch.cuda.synchronize()
+    flush = needs_flush(case)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(i & 0xFF)  # evicts the previous step's data from L2
         step(step_events[i])
     stop.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if rank == 0 else None
-    ms_total = max_over_ranks(start.elapsed_time(stop), world, dev)
+    # with flushes the steps are timed one by one (first phase event to the
+    # event after the replay), so the flushes are not counted
+    mine = (sum(ev[0].elapsed_time(ev[nph]) for ev in step_events) if flush
+            else start.elapsed_time(stop))
+    ms_total = max_over_ranks(mine, world, dev)
     ms_step = ms_total / args.steps
     phase_ms = {name: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_events)
                 for j, name in enumerate(hk.PHASES)}
