@@ -13,8 +13,10 @@ second over the whole step (select + replay), summed over ranks.
 
 Timing: W warm-up steps, then exactly K steps between a barrier +
 synchronize on both sides, CUDA events on the launching stream, max over
-ranks. The inputs of a step (K 128 MiB + Q 64 MiB + the 1 GiB candidate
-buffer) exceed the 129 MB L2, so no flush is added between steps.
+ranks. At the default workload a step touches more than the 129 MB L2
+(K 128 MiB + Q 64 MiB + ~384 MiB of candidates), so no flush is added; for a
+workload whose step would fit in L2 the L2 is flushed before every timed
+step and the steps are timed one by one, without the flushes.
 
 --impl reference times the CPU oracle (test infrastructure, the baseline
 arm) on a bounded sample of the same workload.
@@ -415,9 +417,12 @@ def gpu_arm(args, world, rank, local):
 
 
 def e2e(args, hk, case, dev, ws, world):
-    """Same step through the public API with pinned host inputs: host-to-device
-    copies of every input and device-to-host reads of idx and replay scores are
-    inside the timed region."""
+    """Same step through the public API with pinned host inputs: every step
+    copies all of its inputs host-to-device and reads idx and the replay
+    scores back device-to-host, inside the timed region. The copies run on
+    their own streams, double-buffered, so that step i+1's inputs go up and
+    step i's results come down while step i+1 / step i compute (as a loader
+    that prefetches the next batch would)."""
     import torch
 
     host = {}
@@ -426,37 +431,77 @@ def e2e(args, hk, case, dev, ws, world):
         host[key] = None if a is None else torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     n, H, d = case["q"].shape
     k_top = case["k_top"]
-    out_idx = torch.empty((n, k_top), dtype=torch.int32).pin_memory()
-    out_rs = torch.empty((n, k_top), dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-    d2h = out_idx.numel() * 4 + out_rs.numel() * 4
+    d2h = 2 * n * k_top * 4
+    comp = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dev_in = [{k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in host.items()}
+              for _ in range(2)]
+    dev_idx = [torch.empty((n, k_top), dtype=torch.int32, device=dev) for _ in range(2)]
+    dev_rs = [torch.empty((n, k_top), dtype=torch.float32, device=dev) for _ in range(2)]
+    out_idx = [torch.empty((n, k_top), dtype=torch.int32).pin_memory() for _ in range(2)]
+    out_rs = [torch.empty((n, k_top), dtype=torch.float32).pin_memory() for _ in range(2)]
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    downloaded = [torch.cuda.Event() for _ in range(2)]
 
-    def run():
-        dv = {k: (None if v is None else v.to(dev, non_blocking=True)) for k, v in host.items()}
+    def upload(b):
+        with torch.cuda.stream(up):
+            up.wait_event(computed[b])  # the step that last read buffer b is done
+            for key, v in host.items():
+                if v is not None:
+                    dev_in[b][key].copy_(v, non_blocking=True)
+            uploaded[b].record(up)
+
+    def compute(b):
+        comp.wait_event(uploaded[b])
+        comp.wait_event(downloaded[b])  # the results last in buffer b have left
+        dv = dev_in[b]
         if case["dtype"] == "bf16":
             q = dv["q"].view(torch.int16).view(torch.bfloat16)
             k = dv["k"].view(torch.int16).view(torch.bfloat16)
         else:
             q = dv["q"].view(torch.float8_e4m3fn)
             k = dv["k"].view(torch.float8_e4m3fn)
-        idx, sc, _ = hk.select(q, k, dv["w"], dv["positions"], k_top, q_scale=dv["q_scale"],
-                               k_scale=dv["k_scale"], scores=False, workspace=ws)
-        rs = hk.replay(q, k, dv["w"], idx, q_scale=dv["q_scale"], k_scale=dv["k_scale"])
-        out_idx.copy_(idx, non_blocking=True)
-        out_rs.copy_(rs, non_blocking=True)
+        hk.select(q, k, dv["w"], dv["positions"], k_top, q_scale=dv["q_scale"],
+                  k_scale=dv["k_scale"], scores=False, workspace=ws, out=(dev_idx[b], None))
+        hk.replay(q, k, dv["w"], dev_idx[b], q_scale=dv["q_scale"], k_scale=dv["k_scale"],
+                  out=dev_rs[b])
+        computed[b].record(comp)
 
+    def download(b):
+        with torch.cuda.stream(down):
+            down.wait_event(computed[b])
+            out_idx[b].copy_(dev_idx[b], non_blocking=True)
+            out_rs[b].copy_(dev_rs[b], non_blocking=True)
+            downloaded[b].record(down)
+
+    def run(steps):
+        upload(0)
+        for i in range(steps):
+            b = i & 1
+            compute(b)
+            if i + 1 < steps:
+                upload(b ^ 1)
+            download(b)
+        torch.cuda.synchronize()
+
+    for e in computed + downloaded:
+        e.record(comp)
+    run(2)  # warm-up
     steps = max(1, min(args.steps, 3))
-    run()
-    torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    for _ in range(steps):
-        run()
-    torch.cuda.synchronize()
+    run(steps)
     dt = max_over_ranks((time.perf_counter() - t0) / steps, world, dev)
+    # the last step's results arrived whole
+    if not torch.equal(out_idx[(steps - 1) & 1], dev_idx[(steps - 1) & 1].cpu()):
+        raise RuntimeError("e2e: downloaded indices differ from the device result")
     return {"value": sum_over_ranks(pairs_of(case), world, dev) / dt, "unit": "pairs/s",
             "ms_per_step": dt * 1e3,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "copies": "own streams, double-buffered: next step's inputs up and this step's "
+                      "results down while a step computes"}
 
 
 def twopass(hk, case, t, dev, idx_ref, pairs):
