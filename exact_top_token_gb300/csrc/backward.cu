@@ -7,6 +7,10 @@ namespace hytopk {
 
 cudaError_t launch_backward_bf16(int d, int H, const bwd::BArgs& a, int grid, cudaStream_t st);
 cudaError_t launch_backward_e4m3(int d, int H, const bwd::BArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_backward_bf16_small(int d, int H, const bwd::BArgs& a, int grid,
+                                       cudaStream_t st);
+cudaError_t launch_backward_e4m3_small(int d, int H, const bwd::BArgs& a, int grid,
+                                       cudaStream_t st);
 
 }  // namespace hytopk
 
@@ -21,7 +25,7 @@ extern "C" hytopk_status hytopk_replay_backward(const void* q, const float* q_sc
   hytopk_status s = check_shape(n, L, H, d, k_top, dt);
   if (s != HYTOPK_OK) return s;
   if ((s = check_inputs(q, q_scale, k, k_scale, w, dt, n)) != HYTOPK_OK) return s;
-  if ((H != 16 && H != 32 && H != 64) || (d != 64 && d != 128)) return HYTOPK_UNSUPPORTED;
+  if (H > 64 || (d != 64 && d != 128)) return HYTOPK_UNSUPPORTED;
   if (n == 0) return HYTOPK_OK;
   if (!idx || !grad || !dq || !dk || !dw) return HYTOPK_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(dq) & 15u) || (reinterpret_cast<uintptr_t>(dk) & 15u))
@@ -43,7 +47,10 @@ extern "C" hytopk_status hytopk_replay_backward(const void* q, const float* q_sc
   a.q_e4m3 = dt != HYTOPK_BF16;
   a.status = dev_status;
   const int grid = n < num_sms() ? n : num_sms();
-  const cudaError_t e = dt == HYTOPK_E4M3 ? launch_backward_e4m3(d, H, a, grid, stream)
-                                          : launch_backward_bf16(d, H, a, grid, stream);
+  const bool e4 = dt == HYTOPK_E4M3;
+  const cudaError_t e = H < 16 ? (e4 ? launch_backward_e4m3_small(d, H, a, grid, stream)
+                                     : launch_backward_bf16_small(d, H, a, grid, stream))
+                               : (e4 ? launch_backward_e4m3(d, H, a, grid, stream)
+                                     : launch_backward_bf16(d, H, a, grid, stream));
   return e == cudaSuccess ? HYTOPK_OK : HYTOPK_CUDA_ERROR;
 }

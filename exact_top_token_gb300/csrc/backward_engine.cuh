@@ -72,23 +72,26 @@ struct BArgs {
 
 template <int D, int DT, int H>
 struct Cfg {
+  // heads as the engine sees them: H < 16 runs as 16 heads whose q rows and
+  // weights beyond H are zero (N = 16 is the smallest MMA width here)
+  static constexpr int HP = H < 16 ? 16 : H;
   static constexpr int ES = DT == 0 ? 2 : 1;  // input element bytes
   static constexpr int RB = D * 2;            // bf16 row bytes in shared memory
   static constexpr int DA = RB / 128;         // 128-byte atoms per bf16 row
   static constexpr int STAGES = D == 128 ? 2 : 3;
   static constexpr int KT = 128 * RB;        // bf16 key tile
-  static constexpr int QT = H * RB;          // bf16 q operand of one query
+  static constexpr int QT = HP * RB;         // bf16 q operand of one query
   static constexpr int AT = 128 * 256;       // Aq / Ak: 128 keys x 128 bf16
   static constexpr int RING_OFF = 0;
   static constexpr int Q_OFF = RING_OFF + STAGES * KT;
   static constexpr int AQ_OFF = Q_OFF + 2 * ((QT + 1023) / 1024 * 1024);
   static constexpr int AK_OFF = AQ_OFF + AT;
-  // per query buffer: w [H], q_scale [H] (fp32), then w * q_scale split into
-  // bf16 high / low parts packed two heads per word [H/2] + [H/2]
+  // per query buffer: w [HP], q_scale [HP] (fp32), then w * q_scale split into
+  // bf16 high / low parts packed two heads per word [HP/2] + [HP/2]
   static constexpr int WS_OFF = AK_OFF + AT;
-  static constexpr int DWS_OFF = WS_OFF + 2 * 3 * H * 4;  // dw partials [4][H]
+  static constexpr int DWS_OFF = WS_OFF + 2 * 3 * HP * 4;  // dw partials [4][HP]
   // per epilogue warp: 32 rows x 32 fp32 (row stride 33) for coalescing dk additions
-  static constexpr int TR_OFF = DWS_OFF + 4 * H * 4;
+  static constexpr int TR_OFF = DWS_OFF + 4 * HP * 4;
   static constexpr int TR_FLOATS = 32 * 33;
   static constexpr int BAR_OFF = TR_OFF + kEpiWarps * TR_FLOATS * 4;
   // k_full[S], k_empty[S], q_full[2], q_empty[2], x_full[2], x_empty[2],
@@ -97,11 +100,11 @@ struct Cfg {
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;
   static constexpr int SMEM = MISC_OFF + 16 + 1024;
   // TMEM columns
-  static constexpr int X_COL = 0;           // 2 buffers of H
+  static constexpr int X_COL = 0;           // 2 buffers of HP
   static constexpr int DQ_COL = 128;        // d columns
   static constexpr int DK_COL = 256;        // 2 buffers of d
   static constexpr int CPRS = D * ES / 16;  // 16-byte source chunks per key row
-  static_assert(H == 16 || H == 32 || H == 64, "H");
+  static_assert(H == 1 || H == 2 || H == 4 || H == 8 || H == 16 || H == 32 || H == 64, "H");
   static_assert(D == 64 || D == 128, "d");
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -210,13 +213,14 @@ template <int D, int DT, int H>
 __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
   using C_ = Cfg<D, DT, H>;
   constexpr int STAGES = C_::STAGES, CPRS = C_::CPRS;
+  constexpr int HP = C_::HP;  // heads in shared memory, TMEM and the MMAs (H: in global memory)
   extern __shared__ __align__(1024) uint8_t smem_dyn[];
   uint8_t* smem = tc::align1024(smem_dyn);
   uint8_t* ring = smem + C_::RING_OFF;
   uint8_t* aq = smem + C_::AQ_OFF;
   uint8_t* ak = smem + C_::AK_OFF;
   float* ws = reinterpret_cast<float*>(smem + C_::WS_OFF);     // [qb][w | q_scale | pairs]
-  float* dws = reinterpret_cast<float*>(smem + C_::DWS_OFF);   // [4][H]
+  float* dws = reinterpret_cast<float*>(smem + C_::DWS_OFF);   // [4][HP]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C_::BAR_OFF);
   uint64_t* k_full = bars;
   uint64_t* k_empty = bars + STAGES;
@@ -310,34 +314,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
       const bool q8 = DT == 1 || a.q_e4m3;  // q rows of e4m3 codes
       const int qes = q8 ? 1 : 2;
       const int qch = D * qes / 16;  // 16-byte source chunks per q row
-      for (int f = tid; f < H * qch; f += kProducers) {
+      for (int f = tid; f < HP * qch; f += kProducers) {
         const int h = f / qch, cq = f - h * qch;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-            static_cast<const uint8_t*>(a.q) + ((size_t)t * H + h) * D * qes) + cq);
+        // rows of padded heads (h >= H) are zero
+        const uint8_t* row_src = static_cast<const uint8_t*>(a.q) + ((size_t)t * H + h) * D * qes;
+        const uint4 v = h < H ? __ldg(reinterpret_cast<const uint4*>(row_src) + cq)
+                              : make_uint4(0, 0, 0, 0);
         if (!q8) {
-          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 8, H)) = v;
+          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 8, HP)) = v;
         } else {
           uint4 lo, hi;
           e4m3x16_to_bf16(v, lo, hi);
-          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 16, H)) = lo;
-          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 16 + 8, H)) = hi;
+          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 16, HP)) = lo;
+          *reinterpret_cast<uint4*>(qd + sw_off(h, cq * 16 + 8, HP)) = hi;
         }
       }
-      float* wsq = ws + qb * 3 * H;
-      uint32_t* pairs = reinterpret_cast<uint32_t*>(wsq + 2 * H);
-      for (int h = tid; h < H; h += kProducers) {
-        wsq[h] = a.w[(size_t)t * H + h];
-        wsq[H + h] = q8 ? a.q_scale[(size_t)t * H + h] : 1.0f;
+      float* wsq = ws + qb * 3 * HP;
+      uint32_t* pairs = reinterpret_cast<uint32_t*>(wsq + 2 * HP);
+      for (int h = tid; h < HP; h += kProducers) {
+        wsq[h] = h < H ? a.w[(size_t)t * H + h] : 0.0f;
+        wsq[HP + h] = (q8 && h < H) ? a.q_scale[(size_t)t * H + h] : 1.0f;
       }
-      for (int pr = tid; pr < H / 2; pr += kProducers) {
+      auto head_factor = [&](int h) -> float {  // w * q_scale of head h, 0 if padded
+        if (h >= H) return 0.0f;
+        return a.w[(size_t)t * H + h] * (q8 ? a.q_scale[(size_t)t * H + h] : 1.0f);
+      };
+      for (int pr = tid; pr < HP / 2; pr += kProducers) {
         const int h = 2 * pr;
-        const float s0 = q8 ? a.q_scale[(size_t)t * H + h] : 1.0f;
-        const float s1 = q8 ? a.q_scale[(size_t)t * H + h + 1] : 1.0f;
         uint16_t h0, l0, h1, l1;
-        split_bf16(a.w[(size_t)t * H + h] * s0, h0, l0);
-        split_bf16(a.w[(size_t)t * H + h + 1] * s1, h1, l1);
+        split_bf16(head_factor(h), h0, l0);
+        split_bf16(head_factor(h + 1), h1, l1);
         pairs[pr] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-        pairs[H / 2 + pr] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+        pairs[HP / 2 + pr] = (uint32_t)l0 | ((uint32_t)l1 << 16);
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(q_full + qb);
@@ -393,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      constexpr uint32_t ID_X = tc::instr_desc(0, 128, H);
+      constexpr uint32_t ID_X = tc::instr_desc(0, 128, HP);
       constexpr uint32_t ID_DQ = tc::instr_desc(0, 128, D) | (1u << 15) | (1u << 16);
       constexpr uint32_t ID_DK = tc::instr_desc(0, 128, D) | (1u << 16);
       const uint32_t ring_a = tc::smem_u32(ring), aq_a = tc::smem_u32(aq), ak_a = tc::smem_u32(ak);
@@ -412,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
         for (int j = 0; j < D / 16; ++j) {  // K = d, 16 per step, 32 bytes
           const uint32_t koff = (uint32_t)((j * 32) / 128), kin = (uint32_t)((j * 32) % 128);
           const uint64_t ad = desc2(ring_a + stage * C_::KT + koff * 128 * 128 + kin, 16, 1024);
-          const uint64_t bd = desc2(qa + koff * H * 128 + kin, 16, 1024);
-          tc::mma<0>(tmem_base + C_::X_COL + (g & 1) * H, ad, bd, ID_X, j > 0 ? 1u : 0u);
+          const uint64_t bd = desc2(qa + koff * HP * 128 + kin, 16, 1024);
+          tc::mma<0>(tmem_base + C_::X_COL + (g & 1) * HP, ad, bd, ID_X, j > 0 ? 1u : 0u);
         }
         tc::mma_commit(x_full + (g & 1));
         return true;
@@ -434,13 +442,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           const uint64_t bd = desc2(ring_a + stage * C_::KT + s * 2048, 128 * 128, 1024);
           tc::mma<0>(tmem_base + C_::DQ_COL, ad, bd, ID_DQ, (i > 0 || s > 0) ? 1u : 0u);
         }
-        // DK[key][n] = sum_h' Ak[key][h'] * Q[h' mod H][n]: high then low halves
+        // DK[key][n] = sum_h' Ak[key][h'] * Q[h' mod HP][n]: high then low halves
         const uint32_t qa = tc::smem_u32(q_buf(qi & 1));
 #pragma unroll
-        for (int s = 0; s < 2 * H / 16; ++s) {
+        for (int s = 0; s < 2 * HP / 16; ++s) {
           const uint32_t koff = (uint32_t)((s * 32) / 128), kin = (uint32_t)((s * 32) % 128);
           const uint64_t ad = desc2(ak_a + koff * 128 * 128 + kin, 16, 1024);
-          const uint64_t bd = desc2(qa + (s % (H / 16)) * 2048, H * 128, 1024);
+          const uint64_t bd = desc2(qa + (s % (HP / 16)) * 2048, HP * 128, 1024);
           tc::mma<0>(tmem_base + C_::DK_COL + (g & 1) * D, ad, bd, ID_DK, s > 0 ? 1u : 0u);
         }
         tc::mma_commit(dk_full + (g & 1));
@@ -467,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    constexpr int HG = H / kGroups, DG = D / kGroups;
+    constexpr int HG = HP / kGroups, DG = D / kGroups;
     constexpr int CH = HG < 32 ? HG : 32;       // X columns per TMEM load
     constexpr int NDW = HG >= 32 ? HG / 32 : 1;  // dw sums this lane keeps
     const int h0 = gp * HG, d0 = gp * DG;
@@ -503,9 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
                         tc::mbar_wait(q_full + qb, (qi >> 1) & 1, abort_flag, a.status)))
           break;
       }
-      const float* w_s = ws + qb * 3 * H;
-      const float* qs_s = w_s + H;
-      const uint32_t* vpair = reinterpret_cast<const uint32_t*>(w_s + 2 * H);  // [hi H/2][lo H/2]
+      const float* w_s = ws + qb * 3 * HP;
+      const float* qs_s = w_s + HP;
+      const uint32_t* vpair = reinterpret_cast<const uint32_t*>(w_s + 2 * HP);  // [hi HP/2][lo HP/2]
       const int s = s_next;
       const float G = G_next, ks = ks_next;
       if (g + 1 < total) load_entry(g + 1, s_next, G_next, ks_next);
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
                       tc::mbar_wait(x_full + (g & 1), (g >> 1) & 1, abort_flag, a.status)))
         break;
       tc::fence_after_sync();
-      const uint32_t xaddr = tmem_base + lane_off + C_::X_COL + (g & 1) * H;
+      const uint32_t xaddr = tmem_base + lane_off + C_::X_COL + (g & 1) * HP;
 #pragma unroll
       for (int cc = 0; cc < HG; cc += CH) {
         const int c0 = h0 + cc;
@@ -539,12 +547,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           tc::tmem_ld8(xaddr + c0, x);
           tc::tmem_wait_ld(x);
         }
-        // Aq / Ak rows: 8 heads per 16-byte chunk, high parts at h', low at H + h'
+        // Aq / Ak rows: 8 heads per 16-byte chunk, high parts at h', low at HP + h'
 #pragma unroll
         for (int h8 = 0; h8 < CH; h8 += 8) {
           uint32_t qh[4], ql[4], kh[4], kl[4];
           const uint4 vh = *reinterpret_cast<const uint4*>(vpair + (c0 + h8) / 2);
-          const uint4 vl = *reinterpret_cast<const uint4*>(vpair + H / 2 + (c0 + h8) / 2);
+          const uint4 vl = *reinterpret_cast<const uint4*>(vpair + HP / 2 + (c0 + h8) / 2);
           const uint32_t vhs[4] = {vh.x, vh.y, vh.z, vh.w}, vls[4] = {vl.x, vl.y, vl.z, vl.w};
 #pragma unroll
           for (int u = 0; u < 8; u += 2) {
@@ -558,9 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           }
           const int h = c0 + h8;
           *reinterpret_cast<uint4*>(aq + sw_off(row, h, 128)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
-          *reinterpret_cast<uint4*>(aq + sw_off(row, H + h, 128)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
+          *reinterpret_cast<uint4*>(aq + sw_off(row, HP + h, 128)) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
           *reinterpret_cast<uint4*>(ak + sw_off(row, h, 128)) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
-          *reinterpret_cast<uint4*>(ak + sw_off(row, H + h, 128)) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
+          *reinterpret_cast<uint4*>(ak + sw_off(row, HP + h, 128)) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
         }
         // dw: sum over the warp's 32 keys of G k_scale max(0, X)
 #pragma unroll
@@ -620,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           ok = false;
           break;
         }
-        // DQ: rows h' < H are the high parts, H <= h' < 2H the low parts
+        // DQ: rows h' < HP are the high parts, HP <= h' < 2HP the low parts
         if (!__all_sync(0xffffffffu, tc::mbar_wait(dq_full, qi & 1, abort_flag, a.status))) {
           ok = false;
           break;
@@ -630,18 +638,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
         const uint32_t qaddr = tmem_base + lane_off + C_::DQ_COL + d0;
         // TMEM loads are warp-collective: a warp loads if any of its rows is
         // needed, and each lane then keeps or drops its own row
-        const bool warp_has_lo = quad * 32 < 2 * H && quad * 32 + 32 > H;
-        const bool warp_has_hi = quad * 32 < H;
+        const bool warp_has_lo = quad * 32 < 2 * HP && quad * 32 + 32 > HP;
+        const bool warp_has_hi = quad * 32 < HP;
         if (warp_has_lo) {
 #pragma unroll
           for (int c0 = 0; c0 < DG; c0 += 32) {
             float v[32];
             tc::tmem_ld32(qaddr + c0, v);
             tc::tmem_wait_ld(v);
-            if (row >= H && row < 2 * H) {
+            if (row >= HP && row < 2 * HP) {
 #pragma unroll
               for (int u = 0; u < 32; u += 4)
-                *reinterpret_cast<float4*>(scratch + (row - H) * D + d0 + c0 + u) =
+                *reinterpret_cast<float4*>(scratch + (row - HP) * D + d0 + c0 + u) =
                     make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]);
             }
           }
@@ -650,9 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
 #pragma unroll
         for (int u = 0; u < NDW; ++u) {
           if constexpr (CH >= 32)
-            dws[quad * H + h0 + u * 32 + lane] = dwacc[u];
+            dws[quad * HP + h0 + u * 32 + lane] = dwacc[u];
           else if (lane % (32 / CH) == 0)
-            dws[quad * H + h0 + butterfly_head<CH>(lane, 0)] = dwacc[u];
+            dws[quad * HP + h0 + butterfly_head<CH>(lane, 0)] = dwacc[u];
         }
         if (!__all_sync(0xffffffffu, epi_meet(meet, meet_phase, abort_flag, a.status))) {
           ok = false;
@@ -679,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_backward(const BArgs a) {
           }
         }
         if (gp == 0 && row < H) {
-          const float dsum = (dws[row] + dws[H + row]) + (dws[2 * H + row] + dws[3 * H + row]);
+          const float dsum = (dws[row] + dws[HP + row]) + (dws[2 * HP + row] + dws[3 * HP + row]);
           a.dw[(size_t)t * H + row] = dsum * qs_s[row];
         }
         tc::fence_before_sync();

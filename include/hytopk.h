@@ -56,7 +56,7 @@
  *   - Supported shapes: H in {1,2,4,8,16,32,64,128}; key rows of 64, 128 or
  *     256 bytes, i.e. d in {32, 64, 128} for bf16 and d in {64, 128, 256} for
  *     e4m3; 1 <= k_top <= 16384; n >= 0; L >= 1 (hytopk_replay_backward:
- *     H in {16, 32, 64}, d in {64, 128}). Other shapes return
+ *     H in {1, 2, ..., 64}, d in {64, 128}). Other shapes return
  *     HYTOPK_UNSUPPORTED.
  *   - q and k (and dq, dk of hytopk_replay_backward) must be 16-byte
  *     aligned, every other array 4-byte aligned, so that an array offset by
@@ -228,7 +228,7 @@ HYTOPK_API hytopk_status hytopk_replay_grouped(const void* q, const float* q_sca
  * scale is split into a bf16 high part and a bf16 remainder (about 16
  * significant bits); accumulation is fp32. dk takes floating-point atomic
  * additions, so its low bits depend on the order of arrival.
- *   Supported: H in {16, 32, 64}, d in {64, 128}, both dtypes (others:
+ *   Supported: H in {1, 2, 4, 8, 16, 32, 64}, d in {64, 128}, every dtype (others:
  *   HYTOPK_UNSUPPORTED). dq and dk must be 16-byte aligned.
  *   An index that is not -1 and outside [0, L) contributes nothing and sets
  *   HYTOPK_DEV_REPLAY_BAD_INDEX in *dev_status (device uint32, may be NULL).

@@ -74,6 +74,11 @@ def int_case(L, n, H, d, k_top, dtype, seed):
     (2048, 33, 64, 128, 200, "e4m3"),
     (1500, 20, 16, 64, 129, "e4m3"),
     (1800, 24, 32, 128, 160, "e4m3_bf16"),
+    # fewer than 16 heads (padded to 16 inside the engine)
+    (4096, 64, 4, 64, 256, "bf16"),
+    (2500, 30, 1, 128, 140, "e4m3"),
+    (2200, 26, 2, 64, 170, "bf16"),
+    (1900, 21, 8, 128, 150, "e4m3_bf16"),
 ])
 def test_integer_data_bit_exact(hk, dev, L, n, H, d, k_top, dtype):
     case, g = int_case(L, n, H, d, k_top, dtype, seed=L + n + H)
@@ -98,6 +103,8 @@ def within(gpu, ref, name, rtol=2e-4, eps_amb=True):
     (8192, 40, 64, 128, 1024, "e4m3"),
     (3000, 70, 16, 64, 300, "e4m3"),
     (4000, 30, 64, 128, 400, "e4m3_bf16"),
+    (3500, 45, 4, 64, 256, "bf16"),
+    (3000, 33, 8, 128, 300, "e4m3"),
 ])
 def test_random_data_within_tolerance(hk, dev, L, n, H, d, k_top, dtype):
     case = si.random_case(L, n, H, d, k_top, dtype, seed=7 + n, positions="random")
