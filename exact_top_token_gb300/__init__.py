@@ -18,6 +18,7 @@ from . import _build
 
 __all__ = ["build", "load", "select", "select_twopass", "replay", "select_workspace_size",
            "select_sharded", "select_varlen", "replay_varlen", "replay_backward",
+           "replay_backward_varlen",
            "twopass_workspace_size", "HytopkError", "STATUS", "PHASES", "Stats",
            "symbols"]
 
@@ -36,6 +37,7 @@ symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", 
            "hytopk_select_sharded_workspace_size", "hytopk_select_sharded",
            "hytopk_replay_backward", "hytopk_select_varlen_workspace_size",
            "hytopk_select_varlen", "hytopk_replay_varlen", "hytopk_replay_grouped",
+           "hytopk_replay_backward_varlen",
            "hytopk_status_string", "hytopk_version")
 
 
@@ -105,6 +107,9 @@ def load(path: str | None = None):
                                          P]
     lib.hytopk_replay_varlen.restype = I
     lib.hytopk_replay_varlen.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P]
+    lib.hytopk_replay_backward_varlen.restype = I
+    lib.hytopk_replay_backward_varlen.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P,
+                                                  P, P]
     lib.hytopk_status_string.restype = ctypes.c_char_p
     lib.hytopk_status_string.argtypes = [I]
     lib.hytopk_version.restype = I
@@ -346,6 +351,36 @@ def replay_varlen(q, k, w, idx, cu_q, cu_k, *, q_scale=None, k_scale=None, statu
     if st != 0:
         raise HytopkError(st, "hytopk_replay_varlen")
     return res
+
+
+def replay_backward_varlen(q, k, w, idx, grad, cu_q, cu_k, *, q_scale=None, k_scale=None,
+                           dk=None, status=None, stream=None):
+    """Gradients at the selected entries of a packed variable-length batch
+    (indices relative to each query's sequence): (dq, dk, dw) as
+    :func:`replay_backward`; dk covers all sequences' keys and is added to."""
+    import torch
+
+    lib = load()
+    dt, n, L, H, d, dev = _common(q, q_scale, k, k_scale, w)
+    k_top = idx.shape[1]
+    _check_tensor("idx", idx, dev, torch.int32, (n, k_top))
+    _check_tensor("grad", grad, dev, torch.float32, (n, k_top))
+    cq, ck = _offsets(cu_q, "cu_q"), _offsets(cu_k, "cu_k")
+    if cq.size != ck.size or cq[-1] != n or ck[-1] != L:
+        raise ValueError("cu_q / cu_k do not match the query and key counts")
+    dq = torch.empty((n, H, d), dtype=torch.float32, device=dev)
+    dw = torch.empty((n, H), dtype=torch.float32, device=dev)
+    if dk is None:
+        dk = torch.zeros((L, d), dtype=torch.float32, device=dev)
+    else:
+        _check_tensor("dk", dk, dev, torch.float32, (L, d))
+    st = lib.hytopk_replay_backward_varlen(
+        _ptr(q), _ptr(q_scale), _ptr(k), _ptr(k_scale), _ptr(w), _ptr(idx), _ptr(grad),
+        _cu_ptr(cq), _cu_ptr(ck), cq.size - 1, H, d, k_top, dt, _ptr(dq), _ptr(dk), _ptr(dw),
+        _ptr(status), _stream(dev, stream))
+    if st != 0:
+        raise HytopkError(st, "hytopk_replay_backward_varlen")
+    return dq, dk, dw
 
 
 def read_stats(st) -> dict:

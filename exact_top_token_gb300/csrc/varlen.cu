@@ -1,5 +1,6 @@
 // varlen.cu -- packed variable-length batches: B sequences concatenated along
-// the query and key axes, each selected (or replayed) on its own rows.
+// the query and key axes, each selected, replayed or differentiated on its
+// own rows.
 //
 // Long-context training packs several sequences into one step; every query
 // selects among the keys of its own sequence only (HyScale summary: learned
@@ -144,6 +145,34 @@ extern "C" hytopk_status hytopk_replay_varlen(const void* q, const float* q_scal
                       k_scale ? k_scale + k0 : nullptr, w + (size_t)q0 * H,
                       idx + (size_t)q0 * k_top, nb, Lb, H, d, k_top, dt,
                       scores_out + (size_t)q0 * k_top, dev_status, stream);
+    if (s != HYTOPK_OK) return s;
+  }
+  return HYTOPK_OK;
+}
+
+extern "C" hytopk_status hytopk_replay_backward_varlen(
+    const void* q, const float* q_scale, const void* k, const float* k_scale, const float* w,
+    const int32_t* idx, const float* grad, const int32_t* cu_q, const int32_t* cu_k, int B, int H,
+    int d, int k_top, hytopk_dtype dt, float* dq, float* dk, float* dw, uint32_t* dev_status,
+    cudaStream_t stream) {
+  if (!valid_offsets(cu_q, cu_k, B)) return HYTOPK_INVALID_ARG;
+  const int n = cu_q[B], L = cu_k[B];
+  hytopk_status s = check_shape(n, L > 0 ? L : 1, H, d, k_top, dt);
+  if (s != HYTOPK_OK) return s;
+  if ((s = check_inputs(q, q_scale, k, k_scale, w, dt, n)) != HYTOPK_OK) return s;
+  if (n == 0) return HYTOPK_OK;
+  if (!idx || !grad || !dq || !dk || !dw) return HYTOPK_INVALID_ARG;
+  const size_t qrow = (size_t)H * d * query_bytes(dt), krow = (size_t)d * key_bytes(dt);
+  for (int b = 0; b < B; ++b) {
+    const int q0 = cu_q[b], nb = cu_q[b + 1] - q0, k0 = cu_k[b], Lb = cu_k[b + 1] - k0;
+    if (nb == 0) continue;
+    const size_t e0 = (size_t)q0 * k_top;
+    s = hytopk_replay_backward(static_cast<const uint8_t*>(q) + (size_t)q0 * qrow,
+                               q_scale ? q_scale + (size_t)q0 * H : nullptr,
+                               static_cast<const uint8_t*>(k) + (size_t)k0 * krow,
+                               k_scale ? k_scale + k0 : nullptr, w + (size_t)q0 * H, idx + e0,
+                               grad + e0, nb, Lb, H, d, k_top, dt, dq + (size_t)q0 * H * d,
+                               dk + (size_t)k0 * d, dw + (size_t)q0 * H, dev_status, stream);
     if (s != HYTOPK_OK) return s;
   }
   return HYTOPK_OK;

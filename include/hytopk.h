@@ -357,6 +357,15 @@ HYTOPK_API hytopk_status hytopk_replay_varlen(const void* q, const float* q_scal
                                               hytopk_dtype dt, float* scores_out,
                                               uint32_t* dev_status, cudaStream_t stream);
 
+/* Backward of a packed batch: as hytopk_replay_backward per sequence, with
+ * idx relative to each query's sequence; dq [n, H, d] and dw [n, H] are
+ * written, dk [L, d] (all sequences' keys, concatenated) is added to. */
+HYTOPK_API hytopk_status hytopk_replay_backward_varlen(
+    const void* q, const float* q_scale, const void* k, const float* k_scale, const float* w,
+    const int32_t* idx, const float* grad, const int32_t* cu_q, const int32_t* cu_k, int B, int H,
+    int d, int k_top, hytopk_dtype dt, float* dq, float* dk, float* dw, uint32_t* dev_status,
+    cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 HYTOPK_API const char* hytopk_status_string(hytopk_status status);
 

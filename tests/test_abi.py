@@ -218,3 +218,27 @@ def test_replay_grouped_host_checks(lib):
     assert call(H=3) == 2 and call(d=48) == 2
     assert call(k=P((1 << 20) + 8)) == 5
     assert call(n=0, idx=None) == 0  # nothing to do
+
+
+def test_backward_varlen_host_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(1 << 20)
+
+    def arr(*v):
+        return (ctypes.c_int32 * len(v))(*v)
+
+    def call(**kw):
+        a = dict(q=fake, qs=None, k=fake, ks=None, w=fake, idx=fake, g=fake, cq=arr(0, 3, 7),
+                 ck=arr(0, 100, 250), B=2, H=16, d=64, k_top=8, dt=0, dq=fake, dk=fake, dw=fake,
+                 st=None)
+        a.update(kw)
+        return lib.hytopk_replay_backward_varlen(a["q"], a["qs"], a["k"], a["ks"], a["w"],
+                                                 a["idx"], a["g"], a["cq"], a["ck"], a["B"],
+                                                 a["H"], a["d"], a["k_top"], a["dt"], a["dq"],
+                                                 a["dk"], a["dw"], a["st"], None)
+
+    assert call(cq=arr(0, 5, 3)) == 1  # decreasing offsets
+    assert call(ck=arr(0, 0, 250)) == 1  # a sequence with queries and no keys
+    assert call(g=None) == 1 and call(dk=None) == 1
+    assert call(H=6) == 2
+    assert call(cq=arr(0, 0, 0)) == 0  # no query: nothing to do
