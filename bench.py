@@ -44,6 +44,7 @@ METRIC = ("indexer q-k pairs/s + exact top-k at 1M ctx (% TC peak); "
 REPLAY_BYTES_PER_ENTRY = {  # idx 4 + key row d*esize + key scale + out 4 + q/w share
     "e4m3": 4 + 128 + 4 + 4 + 4.25, "bf16": 4 + 256 + 4 + 4.25}
 WORKLOADS = {"glm_1m": si.glm_1m, "glm_1m_adjacent": si.glm_1m_adjacent,
+             "glm_1m_bf16": si.glm_1m_bf16,
              "mixed_contexts": si.mixed_contexts,
              "tiny_exact": si.tiny_exact}
 # DRAM bytes (read + write) of one full-size filter launch, from the ncu
@@ -273,7 +274,8 @@ def workload_config(case, world=1):
           f"{mib:.0f} MiB per step would fit in the {L2_BYTES // 2**20} MiB L2")
     cfg = {"workload": case["name"], "L": int(case["k"].shape[0]), "n": int(n), "H": int(H),
            "d": int(d), "k_top": int(case["k_top"]), "capacity": 8 * int(case["k_top"]),
-           "positions": "last n" if case["name"] == "glm_1m" else "see synthetic_inputs",
+           "positions": ("last n" if case["name"] in ("glm_1m", "glm_1m_bf16", "glm_1m_adjacent")
+                         else "see synthetic_inputs"),
            "l2": l2}
     if world > 1:
         cfg["parallelism"] = (f"dp{world}: query shards of n per GPU (rank r: the r-th block of n "

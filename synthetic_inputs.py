@@ -146,6 +146,12 @@ def glm_1m(seed: int = 2, L=1 << 20, n=8192, H=64, d=128, k_top=2048):
     return random_case(L, n, H, d, k_top, "e4m3", seed, "last", "normal", name="glm_1m")
 
 
+def glm_1m_bf16(seed: int = 2, L=1 << 20, n=8192, H=64, d=128, k_top=2048):
+    """The glm_1m shapes with bf16 inputs (no scales): the filter's bf16 MMA
+    path at full scale."""
+    return random_case(L, n, H, d, k_top, "bf16", seed, "last", "normal", name="glm_1m_bf16")
+
+
 def glm_1m_adjacent(seed: int = 2, rho: float = 0.98, L=1 << 20, n=8192, H=64, d=128,
                     k_top=2048):
     """glm_1m with neighbouring queries alike (pair_rho = rho): the workload of
