@@ -240,7 +240,7 @@ hytopk_status hytopk_replay_grouped(const void* q, const float* q_scale, const v
 // Two-pass workspace: the per-CTA candidate lists of the read-back kernel, the
 // halved folded weights of the queries (padded by one query block), then the
 // score-table chunk.
-static size_t twopass_lists_bytes(int L) { return align_up((size_t)kRecoveryCtas * L * 8, 1024); }
+static size_t twopass_lists_bytes(int L) { return align_up((size_t)kTableCtas * L * 8, 1024); }
 static size_t twopass_weights_bytes(int n, int H) {
   return align_up(((size_t)n + kQueryPad) * H * 4, 1024);
 }
@@ -294,7 +294,7 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
   for (int row0 = 0; row0 < n; row0 += (int)chunk) {
     const int rows = (int)((size_t)(n - row0) < chunk ? (size_t)(n - row0) : chunk);
     HYTOPK_TRY(launch_table(p, row0, rows, table, hw, dev_status, stream));
-    HYTOPK_TRY(launch_table_topk(p, row0, rows, table, lists, kRecoveryCtas, idx_out, scores_out,
+    HYTOPK_TRY(launch_table_topk(p, row0, rows, table, lists, kTableCtas, idx_out, scores_out,
                                  stream));
   }
   return HYTOPK_OK;

@@ -27,6 +27,7 @@ constexpr int kTileKeys = 128;       // keys per scoring tile (one TMEM lane / t
 constexpr int kQueryPad = 512;       // query slots are padded to a multiple of this
 constexpr int kMaxSamples = 8192;    // upper clamp of the sample count M
 constexpr int kRecoveryCtas = 64;    // persistent CTAs of the recovery kernel (one row each)
+constexpr int kTableCtas = 304;      // CTAs of the two-pass read-back (one row each, 2 per SM)
 constexpr int kMaxTopK = 16384;
 
 // Counters kept in the workspace (zeroed at the start of every call).

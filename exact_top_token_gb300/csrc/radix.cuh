@@ -57,15 +57,19 @@ __device__ __forceinline__ void cta_find_crossing(const uint32_t* hist, int nbin
   __syncthreads();
 }
 
-// Warp-aggregated histogram increment: lanes of a warp that hit the same bin
-// add their count with one shared atomic (scores of a query share their top
-// bits, so without aggregation most increments collide on a few bins). All 32
-// lanes must call it; `active` lanes contribute.
+// Warp-aggregated histogram increment. Scores of a query share their top bits,
+// so most lanes of a warp hit the bin of its first active lane: those add
+// their count with one shared atomic, the others one each. All 32 lanes must
+// call it; `active` lanes contribute.
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin, bool active) {
   const unsigned act = __ballot_sync(0xffffffffu, active);
-  if (!active) return;
-  const unsigned peers = __match_any_sync(act, bin);
-  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(hist + bin, (uint32_t)__popc(peers));
+  if (act == 0u) return;
+  const int first = __ffs(act) - 1;
+  const uint32_t b0 = __shfl_sync(0xffffffffu, bin, first);
+  const bool same = active && bin == b0;
+  const unsigned m = __ballot_sync(0xffffffffu, same);
+  if ((int)(threadIdx.x & 31) == first) atomicAdd(hist + b0, (uint32_t)__popc(m));
+  else if (active && !same) atomicAdd(hist + bin, 1u);
 }
 
 // Shared-memory scratch of the selection helpers.
@@ -195,7 +199,21 @@ static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_
   if (k_eff <= 0) return 0;
   for (int b = threadIdx.x; b < 4096; b += blockDim.x) sc.hist[b] = 0;
   __syncthreads();
-  for (int s0 = 0; s0 < ctx; s0 += blockDim.x) {
+  // rows that start on a 16-byte boundary are read four scores per load
+  // (positions 4i .. 4i+3 by thread i mod blockDim), the rest one per load
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  const int nvec = vec ? ctx / 4 : 0;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  for (int i0 = 0; i0 < nvec; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    const bool in = i < nvec;
+    const float4 v = in ? row4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    hist_add(sc.hist, desc32(v.x) >> 20, in);
+    hist_add(sc.hist, desc32(v.y) >> 20, in);
+    hist_add(sc.hist, desc32(v.z) >> 20, in);
+    hist_add(sc.hist, desc32(v.w) >> 20, in);
+  }
+  for (int s0 = 4 * nvec; s0 < ctx; s0 += blockDim.x) {
     const int s = s0 + threadIdx.x;
     hist_add(sc.hist, s < ctx ? desc32(row[s]) >> 20 : 0u, s < ctx);
   }
@@ -205,14 +223,9 @@ static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_
   if (threadIdx.x == 0) sc.counter = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
-  for (int s0 = 0; s0 < ctx; s0 += blockDim.x) {
-    const int s = s0 + threadIdx.x;
-    float v = 0.0f;
-    bool take = false;
-    if (s < ctx) {
-      v = row[s];
-      take = (desc32(v) >> 20) <= bin;
-    }
+  // list (score, position) of every score in or above the crossing bin
+  auto list_if = [&](float v, int s, bool in) {
+    const bool take = in && (desc32(v) >> 20) <= bin;
     const unsigned mask = __ballot_sync(0xffffffffu, take);
     if (mask) {
       const int leader = __ffs(mask) - 1;
@@ -221,6 +234,20 @@ static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_
       base = __shfl_sync(0xffffffffu, base, leader);
       if (take) list[base + __popc(mask & ((1u << lane) - 1u))] = cand_key(v, s);
     }
+  };
+  for (int i0 = 0; i0 < nvec; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    const bool in = i < nvec;
+    const float4 v = in ? row4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    list_if(v.x, 4 * i, in);
+    list_if(v.y, 4 * i + 1, in);
+    list_if(v.z, 4 * i + 2, in);
+    list_if(v.w, 4 * i + 3, in);
+  }
+  for (int s0 = 4 * nvec; s0 < ctx; s0 += blockDim.x) {
+    const int s = s0 + threadIdx.x;
+    const bool in = s < ctx;
+    list_if(in ? row[s] : 0.0f, s, in);
   }
   __syncthreads();
   const int listed = (int)sc.counter;
