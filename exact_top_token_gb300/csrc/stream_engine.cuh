@@ -62,9 +62,9 @@ struct Cfg {
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NG * QG_BYTES;
   static constexpr int BAR_OFF = K_OFF + STAGES * KT_BYTES;
-  static constexpr int NBARS = 2 * STAGES + 4 + 2;
-  static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;      // tmem base, abort flag
-  static constexpr int POS_OFF = MISC_OFF + 16;
+  static constexpr int NBARS = 2 * STAGES + 4 + 2 + 8;   // + item ring full / empty [4]
+  static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;      // tmem base, abort flag, item ring
+  static constexpr int POS_OFF = MISC_OFF + 32;
   static constexpr int THR_OFF = POS_OFF + QB * 4;
   static constexpr int ROW_OFF = THR_OFF + QB * 4;
   // per-item candidate staging (filter): CAP entries per query slot of the block
@@ -106,6 +106,9 @@ struct Args {
   const float* k_scale;
   int L;
   uint32_t* status;
+  // MODE 0: global item counter (zeroed before the launch); null: items are
+  // dealt round robin (MODE 1, whose items cost the same)
+  uint32_t* work;
 };
 
 __device__ __forceinline__ int find_chunk(const int32_t* off, int nchunks, int item) {
@@ -333,6 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2]
   uint64_t* q_full = bars + 2 * STAGES + 4;
   uint64_t* q_empty = bars + 2 * STAGES + 5;
+  uint64_t* item_full = bars + 2 * STAGES + 6;    // [4]
+  uint64_t* item_empty = bars + 2 * STAGES + 10;  // [4]
+  volatile int32_t* item_ring = reinterpret_cast<volatile int32_t*>(smem + C_::MISC_OFF + 16);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C_::MISC_OFF + 4);
   int32_t* pos_s = reinterpret_cast<int32_t*>(smem + C_::POS_OFF);
@@ -358,6 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(q_full, 1);
     tc::mbar_init(q_empty, 1);
+    for (int i = 0; i < 4; ++i) {
+      tc::mbar_init(item_full + i, 1);
+      tc::mbar_init(item_empty + i, 1 + kEpiWarps);
+    }
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -371,6 +381,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   auto item_at = [&](int i) { return a.reverse ? total - 1 - i : i; };
+  // The n-th item of this CTA. With a work counter (the filter, whose items
+  // differ in cost: the causal edge, candidate appends) the TMA producer takes
+  // the next item from the counter and publishes it through a 4-slot ring that
+  // the MMA issuer and every epilogue warp read in the same order; without
+  // one, items are dealt round robin. An index >= total ends the sequence.
+  auto publish_item = [&](int n) -> int {  // TMA producer lane
+    if (a.work == nullptr) return (int)blockIdx.x + n * (int)gridDim.x;
+    const int slot = n & 3;
+    if (!tc::mbar_wait(item_empty + slot, ((n >> 2) & 1) ^ 1u, abort_flag, a.status)) return -1;
+    const int i = (int)atomicAdd(a.work, 1u);
+    item_ring[slot] = i;
+    tc::mbar_arrive(item_full + slot);
+    return i;
+  };
+  auto take_item = [&](int n) -> int {  // MMA issuer lane, every epilogue lane
+    if (a.work == nullptr) return (int)blockIdx.x + n * (int)gridDim.x;
+    const int slot = n & 3;
+    if (!tc::mbar_wait(item_full + slot, (n >> 2) & 1, abort_flag, a.status)) return -1;
+    return item_ring[slot];
+  };
 
   // Each role starts with its setmaxnreg, so that the register target of its
   // code is the one set there.
@@ -384,7 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t sphase = 0, qphase = 0;
         uint32_t pending = 0, pend_phase = 0, q_loads = 0;  // issued loads, for a clean abort
-        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+        for (int n = 0;; ++n) {
+          const int i = publish_item(n);
+          if (i < 0 || i >= total) break;
           const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
           if (!tc::mbar_wait(q_empty, qphase ^ 1u, abort_flag, a.status)) break;
           qphase ^= 1u;
@@ -440,7 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t k_addr = tc::smem_u32(smem + C_::K_OFF);
         int stage = 0, acc = 0;
         uint32_t sphase = 0, aphase = 0, qphase = 0;
-        for (int i = blockIdx.x; i < total; i += gridDim.x) {
+        for (int n = 0;; ++n) {
+          const int i = take_item(n);
+          if (a.work != nullptr && i >= 0) tc::mbar_arrive(item_empty + (n & 3));
+          if (i < 0 || i >= total) break;
           const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
           if (!tc::mbar_wait(q_full, qphase, abort_flag, a.status)) break;
           qphase ^= 1u;
@@ -509,7 +544,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (MODE == 0 && !REG_META)
       for (int jb = et; jb < QB; jb += kEpiWarps * 32) scnt_s[jb] = 0;
-    for (int i = blockIdx.x; i < total; i += gridDim.x) {
+    for (int n = 0;; ++n) {
+      // every epilogue warp reads the same item sequence (lane 0's view,
+      // after all lanes have read the slot), so the warps stay in step at
+      // the named barriers below
+      const int i = __shfl_sync(0xffffffffu, take_item(n), 0);
+      if (a.work != nullptr && i >= 0) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(item_empty + (n & 3));
+      }
+      if (i < 0 || i >= total) break;
       const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
       epi_sync();
       if (MODE == 0 && !REG_META && prev_block >= 0)

@@ -71,6 +71,7 @@ cudaError_t launch_filter(const Problem& p, const SelectWs& ws, int reverse, cud
   a.k_scale = p.k_scale;
   a.L = p.L;
   a.status = ws.counters + kCtrStatus;
+  a.work = ws.counters + kCtrFilterWork;  // zeroed with the counters at the call's start
   return dispatch(p, 0, km, qm, a, num_sms(), st);
 }
 
