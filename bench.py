@@ -51,7 +51,7 @@ WORKLOADS = {"glm_1m": si.glm_1m, "glm_1m_adjacent": si.glm_1m_adjacent,
 # DRAM bytes (read + write) of one full-size filter launch, from the ncu
 # capture summarised in profiles/glm_1m_launch_list_tensorcore.txt. Must be
 # re-captured (or removed) whenever the filter kernel changes.
-FILTER_TRAFFIC_BYTES = {"glm_1m": 1.0569e9 + 0.3990e9}
+FILTER_TRAFFIC_BYTES = {"glm_1m": 1.0267e9 + 0.3995e9}
 
 
 def parse():
@@ -216,10 +216,31 @@ def oracle_sample(case, rows):
     return sub_pairs, dt
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline(case, n_rows):
     rows = si.sampled_rows(len(case["positions"]), n_rows)
     pairs, dt = oracle_sample(case, rows)
     return {"value": pairs / dt, "unit": "pairs/s", "cores": os.cpu_count(), "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"oracle select of {len(rows)} of {len(case['positions'])} queries "
                       f"({pairs} causal pairs) of {case['name']}, {dt:.1f} s, OpenMP over "
                       "queries on all host cores"}
@@ -244,7 +265,7 @@ def reference_arm(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": case["dtype"],
             "data": "synthetic", "config": workload_config(case),
             "cpu_baseline": {"value": value, "unit": "pairs/s", "cores": os.cpu_count(),
-                             "kind": "oracle",
+                             "kind": "oracle", "cpu": cpu_model(),
                              "sample": f"each step: oracle select of {len(rows)} queries"},
             "e2e": {"value": value, "unit": "pairs/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

@@ -90,15 +90,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but the thread may be suspended (woken when the phase
+// completes) for up to `hint_ns` before the instruction returns false, so a
+// role that waits long (the TMA producer on a full ring, the MMA issuer on
+// busy accumulators) does not take issue slots from the warps that share its
+// scheduler.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 2000;
+
 // Wait until the phase with the given parity of `bar` has completed. Gives up
 // (returns false, raises *abort and the device status bit) after
-// kWaitLimitNs or when another role of the CTA has aborted.
+// kWaitLimitNs or when another role of the CTA has aborted; each retry may
+// suspend the thread for up to kSuspendHintNs, so the abort flag is read at
+// least every 64 * kSuspendHintNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
     if ((i & 63u) == 0) {
       if (*abort) return false;
       if (global_ns() - t0 > kWaitLimitNs) {
