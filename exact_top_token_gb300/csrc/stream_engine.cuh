@@ -156,18 +156,34 @@ __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n
 // multiply, which gives the same value up to the sign of a zero); then the
 // accumulators are combined with packed adds, t = (a0 + a1) + (a2 + a3), and
 // total = lo(t) + hi(t). The sign of a zero total is made +0 by finish_score.
+//
+// With four accumulators, the last one takes its ReLU on the integer pipe
+// instead: for finite x, the signed-integer maximum of x's bit pattern and 0
+// is x when x >= +0 and +0 otherwise. That accumulator then sums ReLU(x) * hw,
+// exactly half of what the (x + |x|) form gives at every step (halving is
+// exact away from the subnormal range), and the combine doubles it exactly:
+// t = (a0 + a1) + (a2 + (a3 + a3)). Splitting the ReLUs between the FMA and
+// ALU pipes this way (one pair in four) shortens the epilogue of the score
+// kernels.
 template <int H>
 struct HeadSum {
   static constexpr int NA = H >= 8 ? 4 : (H >= 2 ? H / 2 : 1);
+  static constexpr bool kAluLast = NA == 4;
   uint64_t a[NA];
   __device__ __forceinline__ void reset() {
 #pragma unroll
     for (int i = 0; i < NA; ++i) a[i] = 0ull;
   }
+  // 2 ReLU(x) for accumulators 0 .. NA-2 (FMA pipe), ReLU(x) for the last
+  // one when kAluLast (integer pipe)
+  __device__ __forceinline__ static float relu_term(int s, float x) {
+    if (kAluLast && s == NA - 1) return __int_as_float(max(__float_as_int(x), 0));
+    return x + fabsf(x);
+  }
   // heads h, h+1 (h even), halved weights hw0, hw1
   __device__ __forceinline__ void add_pair(int h, float x0, float x1, float hw0, float hw1) {
     const int s = (h >> 1) % NA;
-    const float r0 = x0 + fabsf(x0), r1 = x1 + fabsf(x1);
+    const float r0 = relu_term(s, x0), r1 = relu_term(s, x1);
     uint64_t r, w;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(r0), "f"(r1));
     asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(hw0), "f"(hw1));
@@ -177,7 +193,7 @@ struct HeadSum {
   // first pair of an accumulator (h < 2 NA) sets it, so no reset is needed
   __device__ __forceinline__ void add_pair_packed(int h, float x0, float x1, uint64_t w) {
     const int s = (h >> 1) % NA;
-    const float r0 = x0 + fabsf(x0), r1 = x1 + fabsf(x1);
+    const float r0 = relu_term(s, x0), r1 = relu_term(s, x1);
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(r0), "f"(r1));
     if (h < 2 * NA)
@@ -195,8 +211,9 @@ struct HeadSum {
     uint64_t t;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t) : "l"(a[0]), "l"(a[1]));
     if (NA == 4) {
-      uint64_t t23;
-      asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t23) : "l"(a[2]), "l"(a[3]));
+      uint64_t a3x2, t23;
+      asm("add.rn.f32x2 %0, %1, %1;" : "=l"(a3x2) : "l"(a[3]));
+      asm("add.rn.f32x2 %0, %1, %2;" : "=l"(t23) : "l"(a[2]), "l"(a3x2));
       asm("add.rn.f32x2 %0, %0, %1;" : "+l"(t) : "l"(t23));
     }
     float lo, hi;
