@@ -70,7 +70,8 @@ def parse():
                     help="replay of the step: 1 = per query, 2 = adjacent pairs")
     ap.add_argument("--shards", type=int, default=4, help="key ranges of the sharded selection")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=48, help="oracle sample size (queries)")
+    ap.add_argument("--cpu-rows", type=int, default=64,
+                    help="oracle sample size (queries): the first 16, the last 16, 32 evenly spaced")
     ap.add_argument("--queries", type=int, default=0,
                     help="keep only the last N queries of the workload (profiling captures)")
     return ap.parse_args()
