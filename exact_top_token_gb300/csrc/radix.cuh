@@ -150,9 +150,10 @@ static __device__ int cta_select_smallest_u64(const uint64_t* list, int cnt, int
   return k_sel;
 }
 
-// Ascending sort of sel[0..n) in shared memory; entries n..P-1 (P = next
-// power of two) are filled with ~0 and sort last.
-static __device__ void cta_sort_u64(uint64_t* sel, int n) {
+// Ascending bitonic sort of sel[0..n) in shared memory; entries n..P-1 (P =
+// next power of two, within the buffer's capacity) are filled with ~0 and sort
+// last.
+static __device__ void cta_bitonic_u64(uint64_t* sel, int n) {
   int P = 1;
   while (P < n) P <<= 1;
   for (int e = n + threadIdx.x; e < P; e += blockDim.x) sel[e] = ~0ull;
@@ -172,6 +173,135 @@ static __device__ void cta_sort_u64(uint64_t* sel, int n) {
       __syncthreads();
     }
   }
+}
+
+// Ascending sort of sel[0..n) in shared memory (all threads call it; blockDim.x
+// a multiple of 32). With at most 4 keys per thread it is a bucket sort: the
+// upper 32 bits of the keys (the score part of a candidate key), less their
+// minimum, are shifted right until their range fits 4096 ordered buckets, every
+// key is counted, the counts are prefix-summed, each key is scattered into its
+// bucket's range, and its final place in the bucket is the number of the
+// bucket's keys below it (equal keys ordered by their scatter slot). A query's
+// kept scores spread over their range, so a bucket holds a few keys. If a
+// bucket holds more than kMaxBucket keys (many keys sharing a score) or there
+// are more than 4 keys per thread, the bitonic network sorts instead; both
+// give the same order. Uses sc.hist, sc.warp_sums and sc.out.
+static __device__ void cta_sort_u64(uint64_t* sel, int n, RadixScratch& sc) {
+  constexpr int NB = 4096, PER = 4;
+  constexpr uint32_t kMaxBucket = 32;
+  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (n <= 1) {
+    __syncthreads();
+    return;
+  }
+  if (n > PER * T) {
+    cta_bitonic_u64(sel, n);
+    return;
+  }
+  if (tid == 0) {
+    sc.out[0] = 0xffffffffu;
+    sc.out[1] = 0u;
+    sc.out[2] = 0u;
+  }
+  for (int b = tid; b < NB; b += T) sc.hist[b] = 0u;
+  uint64_t key[PER];
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * T;
+    key[r] = i < n ? sel[i] : 0ull;
+    if (i < n) {
+      const uint32_t u = (uint32_t)(key[r] >> 32);
+      lo = min(lo, u);
+      hi = max(hi, u);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  __syncthreads();  // out[] and hist cleared, every key in registers
+  if (lane == 0) {
+    atomicMin(&sc.out[0], lo);
+    atomicMax(&sc.out[1], hi);
+  }
+  __syncthreads();
+  // bucket = (upper - min) >> sh, the smallest shift that maps the range
+  // below NB (so at least NB / 2 buckets are in use when the range is wide)
+  const uint32_t kmin = sc.out[0], range = sc.out[1] - kmin;
+  const int width = range == 0u ? 0 : 32 - __clz(range);
+  const int sh = width > 12 ? width - 12 : 0;
+  int bin[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * T;
+    bin[r] = (int)(((uint32_t)(key[r] >> 32) - kmin) >> sh);
+    if (i < n) atomicAdd(&sc.hist[bin[r]], 1u);
+  }
+  __syncthreads();
+  // exclusive prefix sum of the counts; each thread owns a run of buckets
+  const int per = (NB + T - 1) / T, b0 = tid * per, b1 = min(b0 + per, NB);
+  uint32_t local = 0, big = 0;
+  for (int b = b0; b < b1; ++b) {
+    const uint32_t c = sc.hist[b];
+    local += c;
+    big = max(big, c);
+  }
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+    big = max(big, __shfl_xor_sync(0xffffffffu, big, o));
+  }
+  if (lane == 31) sc.warp_sums[warp] = incl;
+  if (lane == 0) atomicMax(&sc.out[2], big);
+  __syncthreads();
+  uint32_t run = incl - local;
+  for (int w = 0; w < warp; ++w) run += sc.warp_sums[w];
+  for (int b = b0; b < b1; ++b) {
+    const uint32_t c = sc.hist[b];
+    sc.hist[b] = run;
+    run += c;
+  }
+  const bool crowded = sc.out[2] > kMaxBucket;
+  __syncthreads();  // hist[b] = start of bucket b
+  if (crowded) {  // sel is untouched so far
+    cta_bitonic_u64(sel, n);
+    return;
+  }
+  uint32_t slot[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * T;
+    slot[r] = 0u;
+    if (i < n) {
+      slot[r] = atomicAdd(&sc.hist[bin[r]], 1u);
+      sel[slot[r]] = key[r];
+    }
+  }
+  __syncthreads();  // hist[b] = end of bucket b = start of bucket b + 1
+  uint32_t dst[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * T;
+    dst[r] = 0u;
+    if (i < n) {
+      const uint32_t start = bin[r] > 0 ? sc.hist[bin[r] - 1] : 0u, end = sc.hist[bin[r]];
+      uint32_t below = 0;
+      for (uint32_t j = start; j < end; ++j) {
+        const uint64_t o = sel[j];
+        below += (o < key[r] || (o == key[r] && j < slot[r])) ? 1u : 0u;
+      }
+      dst[r] = start + below;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < PER; ++r)
+    if (tid + r * T < n) sel[dst[r]] = key[r];
+  __syncthreads();
 }
 
 // Write one query's sorted selection: k_eff keys then padding to k_top.
@@ -253,7 +383,7 @@ static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_
   const int listed = (int)sc.counter;
   __syncthreads();
   const int got = cta_select_smallest_u64(list, listed, k_eff, sel, sc);
-  cta_sort_u64(sel, got);
+  cta_sort_u64(sel, got, sc);
   return got;
 }
 

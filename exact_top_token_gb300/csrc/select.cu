@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(512) k_select_candidates(Problem p, SelectWs w
   const int cnt = min(ws.cnt[slot], ws.C);
   const int k_eff = min(p.k_top, cnt);
   const int got = cta_select_smallest_u64(ws.cand + (size_t)slot * ws.C, cnt, k_eff, sel, sc);
-  cta_sort_u64(sel, got);
+  cta_sort_u64(sel, got, sc);
   write_selection(sel, got, p.k_top, idx_out + (size_t)t * p.k_top,
                   scores_out ? scores_out + (size_t)t * p.k_top : nullptr);
 }

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(512) k_merge_shards(const int32_t* __restrict_
   int got = 0;
   if (k_eff > 0) {
     got = cta_select_smallest_u64(keys + (size_t)t * P * k_top, used * k_top, k_eff, sel, rsc);
-    cta_sort_u64(sel, got);
+    cta_sort_u64(sel, got, rsc);
   }
   write_selection(sel, got, k_top, idx_out + (size_t)t * k_top,
                   scores_out ? scores_out + (size_t)t * k_top : nullptr);
