@@ -44,6 +44,45 @@ def test_tiny_exact_bit_exact(hk, dev):
     assert stats["device_status"] == 0 and stats["n_queries"] == 64
 
 
+def _desc32_upper(scores):
+    """Upper halves of the selection keys: an unsigned order that is descending score."""
+    u = np.asarray(scores, np.float32).copy()
+    u[u == 0.0] = 0.0
+    u = u.view(np.uint32).astype(np.uint64)
+    asc = np.where(u & 0x80000000, (~u) & 0xFFFFFFFF, u | 0x80000000)
+    return (~asc) & 0xFFFFFFFF
+
+
+def test_sort_ties_inside_buckets(hk, dev):
+    """Integer scores over a wide range: the kept scores of a query are mostly
+    distinct with some exact ties, so the final ordering takes its bucket pass
+    (no bucket above 32 keys) and must order tied scores by position."""
+    case = si.random_case(32768, 32, 16, 64, 2048, dtype="bf16", seed=11, kind="int",
+                          name="int_wide")
+    # weights 1..64: |partial sums| <= 576 * 64 * 16 < 2^24, so scores stay exact
+    case["w"] = si.rng_for(12).integers(1, 65, size=case["w"].shape).astype(np.float32)
+    rows = np.arange(32)
+    ref_idx, ref_sc = oracle.select(case, rows=rows)
+    ties = 0
+    for r in rows:
+        s = ref_sc[r]
+        ties += int(np.sum(s[1:] == s[:-1]))
+        up = _desc32_upper(s)
+        rng = int(up.max() - up.min())
+        sh = max(0, rng.bit_length() - 12)
+        buckets = np.bincount(((up - up.min()) >> np.uint64(sh)).astype(np.int64))
+        assert buckets.max() <= 32  # the bucket pass, not the bitonic fallback
+    assert ties > 100  # tied scores inside buckets, ordered by position
+    idx, sc, _, _ = run_select(hk, case, dev)
+    gi, gs = host(idx, sc)
+    compare(case, rows, gi, gs, exact=True)
+    t = si.to_torch(case, dev)
+    ti, ts = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], case["k_top"],
+                               q_scale=t["q_scale"], k_scale=t["k_scale"])
+    assert np.array_equal(ti.cpu().numpy(), gi)
+    assert np.array_equal(ts.cpu().numpy().view(np.uint32), gs.view(np.uint32))
+
+
 def test_recovery_small_per_row_recovery(hk, dev):
     case = si.recovery_small(oracle.sample_positions)
     C = 8 * case["k_top"]
