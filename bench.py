@@ -514,7 +514,7 @@ def e2e(args, hk, case, dev, ws, world):
     for e in computed + downloaded:
         e.record(comp)
     run(2)  # warm-up
-    steps = max(5, min(args.steps, 10))
+    steps = max(10, min(args.steps, 20))  # pipeline fill and drain spread over 10+ steps
     barrier(world)
     gc.disable()  # no collector pause while the host issues the steps
     t0 = time.perf_counter()
