@@ -249,7 +249,11 @@ HYTOPK_API size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int 
  * beyond each query's position) to the workspace and a second kernel reads
  * them back and selects the exact top-k with the same tie rule and order as
  * hytopk_select. The chunk size is the largest the workspace holds. Same
- * outputs as hytopk_select. */
+ * outputs as hytopk_select, bit for bit. When the whole table is small (a few
+ * hundred MiB: short contexts) this path is the faster of the two, since
+ * writing and reading the table costs less than hytopk_select's sampled
+ * threshold and candidate select; at long contexts hytopk_select is faster
+ * and needs no table. */
 HYTOPK_API hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const void* k,
                                     const float* k_scale, const float* w,
                                     const int32_t* positions, int n, int L, int H, int d,
