@@ -13,8 +13,8 @@
  *               score-table, HyTopK, selection-replay and worked-example
  *               paragraphs.
  *
- * The operation. For query t at position pos[t] (it sees keys s <= pos[t],
- * "every earlier token", Summary) the indexer score is
+ * The operation. For query t at position pos[t] (it sees keys s <= pos[t]:
+ * each query scores all tokens before it, Summary) the indexer score is
  *
  *     I[t,s] = sum_h w[t,h] * ReLU( q[t,h,:] . k[s,:] )
  *
@@ -118,7 +118,8 @@ typedef struct {
 } hytopk_stats;
 
 /* Largest number of failed queries repaired one by one; above it the whole
- * selection is rescored (Explainer, HyTopK paragraph: "more than 64"). */
+ * selection is rescored (Explainer, HyTopK paragraph: the fallback starts
+ * past 64 failed queries). */
 #define HYTOPK_MAX_RECOVERY_ROWS 64
 
 /* Phase boundaries of hytopk_select that hytopk_select_ex can time. */
