@@ -19,7 +19,7 @@
  *
  * What is computed (readings of the pages are marked READING):
  *   ctx(t) = positions[t] + 1: query t sees keys s <= positions[t]
- *     ("scores every earlier token", Summary, What the paper found).
+ *     (each query scores all tokens before it: Summary, What the paper found).
  *   I[t,s] = sum_h w[t,h] * max(0, dot_h),  dot_h = sum_i q[t,h,i] * k[s,i]
  *     READING: the DeepSeek-style indexer score (Summary names DeepSeek-style
  *     token selection; Explainer, score-table paragraph, calls it attention-
