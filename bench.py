@@ -44,14 +44,49 @@ METRIC = ("indexer q-k pairs/s + exact top-k at 1M ctx (% TC peak); "
           "replay entries/s (% HBM)")
 REPLAY_BYTES_PER_ENTRY = {  # idx 4 + key row d*esize + key scale + out 4 + q/w share
     "e4m3": 4 + 128 + 4 + 4 + 4.25, "bf16": 4 + 256 + 4 + 4.25}
+
+
+def recovery_stress():
+    """The recovery-stress workload, its sample positions taken from the
+    library's own sample plan (the same formulas its kernels use)."""
+    import exact_top_token_gb300 as hk
+
+    hk.build()
+    hk.load()
+    return si.recovery_stress(lambda ctx: hk.sample_plan(ctx, 1)[0])
+
+
 WORKLOADS = {"glm_1m": si.glm_1m, "glm_1m_adjacent": si.glm_1m_adjacent,
              "glm_1m_bf16": si.glm_1m_bf16,
              "mixed_contexts": si.mixed_contexts,
+             "recovery_stress": recovery_stress,
              "tiny_exact": si.tiny_exact}
-# DRAM bytes (read + write) of one full-size filter launch, from the ncu
-# capture summarised in profiles/glm_1m_launch_list_tensorcore.txt. Must be
-# re-captured (or removed) whenever the filter kernel changes.
-FILTER_TRAFFIC_BYTES = {"glm_1m": 1.0188e9 + 0.3980e9}
+# DRAM bytes (read + write) of one full-size filter launch, from one ncu
+# capture of the filter kernel at the build named beside it (its launch list is
+# summarised under profiles/). Reported as roofline.traffic only while the
+# running library is that build (the source digest below matches); otherwise
+# the traffic is reported as null.
+FILTER_TRAFFIC = {"glm_1m": {"bytes": 1.0188e9 + 0.3980e9, "build": None}}
+FILTER_SOURCES = ("stream_engine.cuh", "stream_launch.cu", "stream_d128_e4m3.cu", "tc.cuh",
+                  "common.cuh")
+
+
+def filter_source_digest():
+    """sha256 (first 12 hex digits) of the filter kernel's source files."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in FILTER_SOURCES:
+        with open(os.path.join(ROOT, "exact_top_token_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def filter_traffic(workload):
+    rec = FILTER_TRAFFIC.get(workload)
+    if rec is None or rec["build"] != filter_source_digest():
+        return None
+    return rec["bytes"]
 
 
 def parse():
@@ -66,6 +101,8 @@ def parse():
     ap.add_argument("--no-sharded", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-grouped", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the mixed-context and recovery-stress sections")
     ap.add_argument("--replay-group", type=int, default=1, choices=[1, 2],
                     help="replay of the step: 1 = per query, 2 = adjacent pairs")
     ap.add_argument("--shards", type=int, default=4, help="key ranges of the sharded selection")
@@ -337,65 +374,14 @@ def gpu_arm(args, world, rank, local):
     dt_code = hk.E4M3 if case["dtype"] == "e4m3" else hk.BF16
     ws = torch.empty(hk.select_workspace_size(n, L, H, d, k_top, 0, dt_code), dtype=torch.uint8,
                      device=dev)
-    idx = torch.empty((n, k_top), dtype=torch.int32, device=dev)
-    sc = torch.empty((n, k_top), dtype=torch.float32, device=dev)
-    rs = torch.empty((n, k_top), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    nph = len(hk.PHASES) + 1
-    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
-                   for _ in range(args.steps)]
-    # torch creates CUDA events lazily: record each once so that the handles
-    # exist before the library records them on the stream
-    for evs in step_events:
-        for e in evs:
-            e.record(stream)
-    torch.cuda.synchronize()
-
-    def step(events=None):
-        hk.select(t["q"], t["k"], t["w"], t["positions"], k_top, q_scale=t["q_scale"],
-                  k_scale=t["k_scale"], workspace=ws, out=(idx, sc),
-                  phase_events=None if events is None else events[:nph])
-        hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"],
-                  group=args.replay_group,
-                  out=rs)
-        if events is not None:
-            events[nph].record(stream)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
     clocks = ClockSampler()
     if rank == 0:
         clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    flush = needs_flush(case)
-    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for i in range(args.steps):
-        if flush:
-            flush_buf.fill_(i & 0xFF)  # evicts the previous step's data from L2
-        step(step_events[i])
-    stop.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    tm = time_steps(hk, case, t, ws, dev, args.steps, args.warmup, args.replay_group, world)
     clk = clocks.stop() if rank == 0 else None
-    # with flushes the steps are timed one by one (first phase event to the
-    # event after the replay), so the flushes are not counted
-    mine = (sum(ev[0].elapsed_time(ev[nph]) for ev in step_events) if flush
-            else start.elapsed_time(stop))
-    ms_total = max_over_ranks(mine, world, dev)
-    ms_step = ms_total / args.steps
-    phase_ms = {name: statistics.mean(ev[j].elapsed_time(ev[j + 1]) for ev in step_events)
-                for j, name in enumerate(hk.PHASES)}
-    replay_ms = statistics.mean(ev[nph - 1].elapsed_time(ev[nph]) for ev in step_events)
-    select_ms = statistics.mean(ev[0].elapsed_time(ev[nph - 1]) for ev in step_events)
-
-    # correctness guard: replay reproduces the selected scores bit for bit
-    if not torch.equal(rs, sc):
-        raise RuntimeError("replayed scores differ from the selected scores")
+    idx, sc = tm["idx"], tm["scores"]
+    ms_step = tm["ms_step"]
+    phase_ms, replay_ms, select_ms = tm["phases_ms"], tm["replay_ms"], tm["select_ms"]
 
     pk = peaks()
     flops_per_pair = 2 * H * d
@@ -407,8 +393,9 @@ def gpu_arm(args, world, rank, local):
     roofline = {"kernel": "k_stream filter (fused score + threshold filter)", "bound": "tensor",
                 "achieved": achieved_tflops, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved_tflops / peak,
-                "traffic": (None if args.queries else FILTER_TRAFFIC_BYTES.get(args.workload)),
-                "traffic_unit": "bytes per launch (ncu dram read + write)",
+                "traffic": (None if args.queries else filter_traffic(args.workload)),
+                "traffic_unit": ("bytes per launch (ncu dram read + write of the filter "
+                                 "build with source digest " + filter_source_digest() + ")"),
                 "algorithmic_flops_per_launch": pairs * flops_per_pair,
                 "peak_source": (f"{'2 x ' if case['dtype'] == 'e4m3' else ''}measured bf16 burst "
                                 f"{pk['bf16_tflops']} TFLOP/s ({pk['source']})")}
@@ -435,10 +422,135 @@ def gpu_arm(args, world, rank, local):
         line["grouped_replay"] = grouped(hk, case, t, dev, idx, ws, args, pk)
     if not args.no_backward and H in (16, 32, 64):
         line["backward"] = backward(hk, case, t, dev, idx, pk)
+    if (not args.no_workloads and world == 1 and args.workload == "glm_1m"
+            and not args.queries):
+        del t, ws, idx, sc, tm
+        torch.cuda.empty_cache()
+        line["workloads"] = {name: side_workload(hk, name, dev, pk)
+                             for name in ("mixed_contexts", "recovery_stress")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_rows)
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_steps(hk, case, t, ws, dev, steps, warmup, replay_group=1, world=1, stats=False):
+    """`warmup` untimed steps, then `steps` timed ones (select + replay), with
+    the library's phase events around each phase. When a step's data would fit
+    in the L2, the L2 is flushed before every timed step and the steps are
+    timed one by one (first phase event to the event after the replay), so
+    the flushes are not counted; otherwise the whole run is timed between
+    barrier + synchronize. Returns the mean times, the last step's outputs
+    and, on request, its statistics."""
+    import torch
+
+    n, H, d = case["q"].shape
+    k_top = case["k_top"]
+    idx = torch.empty((n, k_top), dtype=torch.int32, device=dev)
+    sc = torch.empty((n, k_top), dtype=torch.float32, device=dev)
+    rs = torch.empty((n, k_top), dtype=torch.float32, device=dev)
+    st = torch.zeros(8, dtype=torch.int32, device=dev) if stats else None
+    stream = torch.cuda.current_stream(dev)
+    nph = len(hk.PHASES) + 1
+    step_events = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
+                   for _ in range(steps)]
+    # torch creates CUDA events lazily: record each once so that the handles
+    # exist before the library records them on the stream
+    for evs in step_events:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    def step(events=None):
+        _, _, st_out = hk.select(t["q"], t["k"], t["w"], t["positions"], k_top,
+                                 q_scale=t["q_scale"], k_scale=t["k_scale"], workspace=ws,
+                                 out=(idx, sc), stats=False,
+                                 phase_events=None if events is None else events[:nph])
+        hk.replay(t["q"], t["k"], t["w"], idx, q_scale=t["q_scale"], k_scale=t["k_scale"],
+                  group=replay_group, out=rs)
+        if events is not None:
+            events[nph].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    flush = needs_flush(case)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        if flush:
+            flush_buf.fill_(i & 0xFF)  # evicts the previous step's data from L2
+        step(step_events[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    mine = (sum(ev[0].elapsed_time(ev[nph]) for ev in step_events) if flush
+            else start.elapsed_time(stop))
+    ms_total = max_over_ranks(mine, world, dev)
+    out = {"ms_step": ms_total / steps, "flushed": flush,
+           "phases_ms": {name: statistics.mean(ev[j].elapsed_time(ev[j + 1])
+                                               for ev in step_events)
+                         for j, name in enumerate(hk.PHASES)},
+           "replay_ms": statistics.mean(ev[nph - 1].elapsed_time(ev[nph]) for ev in step_events),
+           "select_ms": statistics.mean(ev[0].elapsed_time(ev[nph - 1]) for ev in step_events),
+           "idx": idx, "scores": sc}
+    # correctness guard: replay reproduces the selected scores bit for bit
+    if not torch.equal(rs.view(torch.int32), sc.view(torch.int32)):
+        raise RuntimeError("replayed scores differ from the selected scores")
+    if stats:
+        _, _, st = hk.select(t["q"], t["k"], t["w"], t["positions"], k_top,
+                             q_scale=t["q_scale"], k_scale=t["k_scale"], workspace=ws,
+                             out=(idx, sc), stats=True)
+        out["stats"] = hk.read_stats(st)
+    del flush_buf
+    return out
+
+
+def side_workload(hk, name, dev, pk, steps=10, warmup=3):
+    """One of the other workloads timed like the headline one (select + replay
+    per step, phase events): mixed contexts (64K keys, queries at evenly
+    spaced positions, some with fewer keys than k) and recovery stress (256K
+    keys, more than 64 failed queries, so every query is rescored over its
+    whole context). The in-library two-pass path is timed beside them."""
+    import torch
+
+    case = WORKLOADS[name]()
+    n, H, d = case["q"].shape
+    L = case["k"].shape[0]
+    k_top = case["k_top"]
+    t = si.to_torch(case, dev)
+    dt_code = hk.E4M3 if case["dtype"] == "e4m3" else hk.BF16
+    ws = torch.empty(hk.select_workspace_size(n, L, H, d, k_top, 0, dt_code), dtype=torch.uint8,
+                     device=dev)
+    tm = time_steps(hk, case, t, ws, dev, steps, warmup, stats=True)
+    pairs = pairs_of(case)
+    flops = pairs * 2 * H * d
+    peak = pk["bf16_tflops"] * (2.0 if case["dtype"] == "e4m3" else 1.0)
+    filt = tm["phases_ms"]["filter"]
+    res = {"config": workload_config(case), "dtype": case["dtype"], "steps": steps,
+           "warmup": warmup, "ms_per_step": tm["ms_step"],
+           "pairs_per_s": pairs / (tm["ms_step"] / 1e3), "select_ms": tm["select_ms"],
+           "replay_ms": tm["replay_ms"], "phases_ms": tm["phases_ms"],
+           "filter": {"tflops": flops / (filt / 1e3) / 1e12, "peak_tflops": peak,
+                      "frac": flops / (filt / 1e3) / 1e12 / peak},
+           "stats": tm["stats"],
+           "replay_entries_per_s": n * k_top / (tm["replay_ms"] / 1e3)}
+    if name == "recovery_stress":
+        st = tm["stats"]
+        res["recovery"] = {"ms": tm["phases_ms"]["recover"], "n_failed": st["n_failed"],
+                           "fallback_used": st["fallback_used"],
+                           "rescored_pairs_per_s": (pairs / (tm["phases_ms"]["recover"] / 1e3)
+                                                    if st["fallback_used"] else None)}
+    tp = twopass(hk, case, t, dev, tm["idx"], pairs)
+    res["twopass"] = {"select_ms": tp["ms"], "same_idx_as_hytopk": tp["same_idx_as_hytopk"],
+                      "hytopk_select_ms": tm["select_ms"]}
+    del t, ws, tm
+    torch.cuda.empty_cache()
+    return res
 
 
 def e2e(args, hk, case, dev, ws, world):

@@ -19,7 +19,7 @@ from . import _build
 __all__ = ["build", "load", "select", "select_twopass", "replay", "select_workspace_size",
            "select_sharded", "select_varlen", "replay_varlen", "replay_backward",
            "replay_backward_varlen",
-           "twopass_workspace_size", "HytopkError", "STATUS", "PHASES", "Stats",
+           "twopass_workspace_size", "sample_plan", "HytopkError", "STATUS", "PHASES", "Stats",
            "symbols"]
 
 MAX_RECOVERY_ROWS = 64
@@ -29,6 +29,7 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or dtype",
 DEV_REPLAY_BAD_INDEX = 0x1
 DEV_BAD_SCALE = 0x2
 DEV_BAD_POSITION = 0x4
+DEV_WAIT_TIMEOUT = 0x80000000  # a bounded wait gave up: the call's outputs are undefined
 BF16, E4M3, E4M3_BF16 = 0, 1, 2  # E4M3_BF16: e4m3 q (with q_scale), bf16 k
 
 # the C-ABI symbols declared in include/hytopk.h
@@ -37,7 +38,7 @@ symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", 
            "hytopk_select_sharded_workspace_size", "hytopk_select_sharded",
            "hytopk_replay_backward", "hytopk_select_varlen_workspace_size",
            "hytopk_select_varlen", "hytopk_replay_varlen", "hytopk_replay_grouped",
-           "hytopk_replay_backward_varlen",
+           "hytopk_replay_backward_varlen", "hytopk_sample_plan",
            "hytopk_status_string", "hytopk_version")
 
 
@@ -110,6 +111,8 @@ def load(path: str | None = None):
     lib.hytopk_replay_backward_varlen.restype = I
     lib.hytopk_replay_backward_varlen.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, P,
                                                   P, P]
+    lib.hytopk_sample_plan.restype = ctypes.c_int32
+    lib.hytopk_sample_plan.argtypes = [ctypes.c_int64, ctypes.c_int32, P, P]
     lib.hytopk_status_string.restype = ctypes.c_char_p
     lib.hytopk_status_string.argtypes = [I]
     lib.hytopk_version.restype = I
@@ -176,6 +179,19 @@ def _common(q, q_scale, k, k_scale, w):
     _check_tensor("q_scale", q_scale, dev, torch.float32, (n, H))
     _check_tensor("k_scale", k_scale, dev, torch.float32, (L,))
     return dt, n, L, H, d, dev
+
+
+def sample_plan(ctx: int, k_top: int):
+    """(positions, r): the sample positions of a query with ctx visible keys
+    and the rank of its threshold among them (host computation in the library)."""
+    import numpy as np
+
+    lib = load()
+    out = np.zeros(8192, dtype=np.int32)
+    r = ctypes.c_int32(0)
+    m = lib.hytopk_sample_plan(int(ctx), int(k_top), out.ctypes.data_as(ctypes.c_void_p),
+                               ctypes.byref(r))
+    return out[:m].copy(), int(r.value)
 
 
 def select_workspace_size(n, L, H, d, k_top, capacity=0, dtype=BF16) -> int:

@@ -300,6 +300,16 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
   return HYTOPK_OK;
 }
 
+int32_t hytopk_sample_plan(int64_t ctx, int32_t k_top, int32_t* positions_out,
+                           int32_t* rank_out) {
+  if (ctx < 1 || k_top < 1) return 0;
+  const int m = sample_count(ctx);
+  if (positions_out)
+    for (int j = 0; j < m; ++j) positions_out[j] = sample_position(ctx, m, j);
+  if (rank_out) *rank_out = threshold_rank(ctx, k_top, m);
+  return m;
+}
+
 const char* hytopk_status_string(hytopk_status status) {
   switch (status) {
     case HYTOPK_OK: return "ok";

@@ -168,19 +168,19 @@ __device__ __forceinline__ uint64_t cand_key(float score, int32_t pos) {
 
 // ---- threshold parameters (HyScale explainer: HyTopK paragraph, worked example) ----
 
-__device__ __forceinline__ int sample_count(int64_t ctx) {
+__host__ __device__ __forceinline__ int sample_count(int64_t ctx) {
   int64_t m = ctx / 128;
   m = m < 4096 ? 4096 : m;
   m = m > kMaxSamples ? kMaxSamples : m;
   return (int)(m < ctx ? m : ctx);
 }
 
-__device__ __forceinline__ int threshold_rank(int64_t ctx, int64_t k, int m) {
+__host__ __device__ __forceinline__ int threshold_rank(int64_t ctx, int64_t k, int m) {
   int64_t r = (3 * k * (int64_t)m + ctx - 1) / ctx;
   return (int)(r < m ? r : m);
 }
 
-__device__ __forceinline__ int sample_position(int64_t ctx, int m, int j) {
+__host__ __device__ __forceinline__ int sample_position(int64_t ctx, int m, int j) {
   return (int)(((int64_t)j * ctx) / m);
 }
 

@@ -18,7 +18,7 @@
 // library routine is called.
 #include <mutex>
 
-#include "hytopk.h"
+#include "launch.h"
 
 namespace {
 
@@ -52,10 +52,15 @@ extern "C" hytopk_status hytopk_select_noalloc(const void* q, const float* q_sca
                                                int d, int k_top, hytopk_dtype dt,
                                                int32_t* idx_out, float* scores_out, int capacity,
                                                hytopk_stats* stats_out, cudaStream_t stream) {
+  // the argument checks of hytopk_select, in its order, before the size check
+  hytopk_status s = hytopk::check_shape(n, L, H, d, k_top, dt);
+  if (s != HYTOPK_OK) return s;
+  s = hytopk::check_inputs(q, q_scale, k, k_scale, w, dt, n);
+  if (s != HYTOPK_OK) return s;
+  if (capacity < 0 || (capacity > 0 && capacity < k_top)) return HYTOPK_INVALID_ARG;
+  if (n > 0 && (!positions || !idx_out)) return HYTOPK_INVALID_ARG;
   const size_t need = hytopk_select_workspace_size(n, L, H, d, k_top, capacity, dt);
-  if (need == 0)  // invalid or unsupported arguments: let hytopk_select report which
-    return hytopk_select(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt, idx_out,
-                         scores_out, capacity, nullptr, 0, stats_out, stream);
+  if (need == 0) return HYTOPK_INVALID_ARG;
   if (need > kScratchBytes) return HYTOPK_WORKSPACE_TOO_SMALL;
   void* scratch = scratch_on_current_device();
   if (!scratch) return HYTOPK_CUDA_ERROR;

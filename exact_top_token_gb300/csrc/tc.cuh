@@ -19,7 +19,7 @@ namespace tc {
 
 // Device status bit set when a bounded wait gives up (a kernel bug or a stall:
 // the kernel then stops its loops, frees its TMEM and returns).
-constexpr uint32_t kDevTimeout = 0x80000000u;
+constexpr uint32_t kDevTimeout = HYTOPK_DEV_WAIT_TIMEOUT;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -101,6 +101,10 @@ typedef enum { HYTOPK_BF16 = 0, HYTOPK_E4M3 = 1, HYTOPK_E4M3_BF16 = 2 } hytopk_d
 #define HYTOPK_DEV_REPLAY_BAD_INDEX 0x1u /* replay index not -1 and outside [0, L): entry is NaN */
 #define HYTOPK_DEV_BAD_SCALE 0x2u        /* a q_scale or k_scale <= 0 (results undefined) */
 #define HYTOPK_DEV_BAD_POSITION 0x4u     /* a position outside [0, L): that query is all -1 */
+/* A bounded wait inside a tensor-core kernel gave up (after 2 s): the kernel
+ * stopped its loops, freed its tensor memory and returned, so every output of
+ * that call is undefined. It signals a stalled GPU or a library bug. */
+#define HYTOPK_DEV_WAIT_TIMEOUT 0x80000000u
 
 /* Per-call statistics of hytopk_select (device memory, written at the end of
  * the call's stream work). The check kernel flags a query with ctx > k whose
@@ -146,6 +150,19 @@ typedef struct {
   int reverse_schedule;
   int reserved;
 } hytopk_select_options;
+
+/* The evenly spaced samples of a query with ctx = pos + 1 visible keys
+ * (Explainer, HyTopK paragraph and worked example): returns the sample count
+ *     M = min(ctx, max(4096, floor(ctx / 128)), 8192)
+ * and, when the pointers are not NULL, writes the sample positions
+ * p_j = floor(j * ctx / M), j = 0 .. M-1, to positions_out (HOST memory, room
+ * for M <= 8192 entries) and the threshold rank r = min(M, ceil(3 k M / ctx))
+ * to *rank_out (host). The threshold of the query is the r-th best score
+ * among its samples. A query with ctx <= k_top keeps all its keys and uses no
+ * samples. Host-only: no CUDA call. Returns 0 (writing nothing) when ctx < 1
+ * or k_top < 1. These are the same integer formulas the kernels use. */
+HYTOPK_API int32_t hytopk_sample_plan(int64_t ctx, int32_t k_top, int32_t* positions_out,
+                                      int32_t* rank_out);
 
 /* Bytes of workspace hytopk_select needs. capacity = candidate buffer slots
  * per query (0 selects the default 8 * k_top). Returns 0 for invalid or
@@ -276,8 +293,10 @@ HYTOPK_API hytopk_status hytopk_select_twopass(const void* q, const float* q_sca
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture.
- *   A problem whose hytopk_select_workspace_size exceeds the array returns
- *   HYTOPK_WORKSPACE_TOO_SMALL and launches nothing.
+ *   Argument errors are reported as by hytopk_select (shape, then pointers
+ *   and alignment); only then does a problem whose
+ *   hytopk_select_workspace_size exceeds the array return
+ *   HYTOPK_WORKSPACE_TOO_SMALL, launching nothing.
  *   All calls share the one array and each call overwrites it (the call
  *   itself clears what must start at zero), so calls whose GPU work overlaps
  *   in time -- on different streams or host threads -- race; the caller must

@@ -16,6 +16,52 @@ import oracle
 import synthetic_inputs as si
 
 REL_TOL = 1e-3
+# A score smaller than 2^-10 of the sum of the magnitudes of its terms has lost
+# ten bits or more to cancellation; there "1e-3 relative" is taken relative to
+# that sum / 1024 instead (see replay_tolerance).
+CANCEL_FLOOR = 2.0 ** -10
+
+
+def decoded(case):
+    """q [n,H,d] and k [L,d] as fp64 values (element code times its row scale)."""
+    qdt, kdt = si.element_types(case["dtype"])
+    table = oracle.e4m3_table().astype(np.float64)
+
+    def dec(a, dt, scale):
+        v = (si.bf16_bits_to_f32(a).astype(np.float64) if dt == "bf16" else table[a])
+        if scale is not None:
+            v = v * np.asarray(scale, np.float64)[..., None]
+        return v
+
+    return dec(case["q"], qdt, case["q_scale"]), dec(case["k"], kdt, case["k_scale"])
+
+
+def abs_term_sum(case, idx):
+    """B[t,j] = sum_h |w[t,h]| * sum_i |q[t,h,i]| |k[idx[t,j],i]| (fp64): the sum
+    of the magnitudes of every product that enters the score of entry (t, j).
+    Entries with idx outside [0, L) get 0."""
+    q, k = decoded(case)
+    L = k.shape[0]
+    idx = np.asarray(idx)
+    out = np.zeros(idx.shape, np.float64)
+    aq, ak, aw = np.abs(q), np.abs(k), np.abs(np.asarray(case["w"], np.float64))
+    for t in range(idx.shape[0]):
+        ok = (idx[t] >= 0) & (idx[t] < L)
+        if ok.any():
+            out[t, ok] = aw[t] @ (aq[t] @ ak[idx[t, ok]].T)
+    return out
+
+
+def replay_tolerance(case, idx, ref):
+    """Per-entry tolerance of a replayed score: 1e-3 relative to
+    max(|ref|, CANCEL_FLOOR * B) with B = abs_term_sum. Both sides evaluate the
+    score in fp32 (a dot of d products, then a weighted sum of H terms); their
+    rounding errors scale with B, not with the possibly cancelled result
+    (about sqrt(d + H) * 2^-24 * B each, i.e. < 1e-6 B at d + H = 192), so
+    below B / 1024 the relative error of a correct fp32 evaluation is not
+    bounded by 1e-3. Selected (top-k) entries sit far above the floor."""
+    B = abs_term_sum(case, idx)
+    return REL_TOL * np.maximum(np.abs(ref).astype(np.float64), CANCEL_FLOOR * B)
 
 
 def check_structure(idx, scores, positions, k_top):

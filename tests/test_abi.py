@@ -242,3 +242,63 @@ def test_backward_varlen_host_checks(lib):
     assert call(g=None) == 1 and call(dk=None) == 1
     assert call(H=6) == 2
     assert call(cq=arr(0, 0, 0)) == 0  # no query: nothing to do
+
+
+def test_wait_timeout_bit_matches_the_header():
+    text = open(os.path.join(ROOT, "include", "hytopk.h")).read()
+    m = re.search(r"#define HYTOPK_DEV_WAIT_TIMEOUT (0x[0-9a-fA-F]+)u", text)
+    assert m and int(m.group(1), 16) == hk.DEV_WAIT_TIMEOUT
+
+
+def test_sample_plan_equals_the_oracle(lib):
+    """The library's host-side sample plan (sample count M, positions p_j and
+    threshold rank r of a query with ctx keys) against the oracle's, at the
+    clamp boundaries of M and at the 1M-key setting."""
+    import numpy as np
+
+    import oracle
+
+    ctxs = [1, 2, 3, 100, 255, 256, 257, 2047, 2048, 2049, 4095, 4096, 4097, 6000, 65535,
+            524287, 524288, 524289, 1000003, 1 << 20, (1 << 20) + 1, 1 << 24, (1 << 30) - 1]
+    for k_top in (1, 256, 2048, 16384):
+        for ctx in ctxs:
+            pos, r = hk.sample_plan(ctx, k_top)
+            m = oracle.sample_count(ctx)
+            assert len(pos) == m
+            assert r == oracle.threshold_rank(ctx, k_top)
+            assert np.array_equal(pos, oracle.sample_positions(ctx).astype(np.int32)), ctx
+    # the worked example at 1M keys: 8192 samples, 128 keys apart, the 48th best
+    pos, r = hk.sample_plan(1 << 20, 2048)
+    assert len(pos) == 8192 and r == 48 and np.all(np.diff(pos) == 128)
+    assert lib.hytopk_sample_plan(0, 2048, None, None) == 0
+    assert lib.hytopk_sample_plan(5000, 0, None, None) == 0
+
+
+def test_noalloc_host_checks(lib):
+    """hytopk_select_noalloc reports argument errors as hytopk_select does,
+    before its scratch-size check, without touching the device."""
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f = lib.hytopk_select_noalloc
+    f.restype = I
+    f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, P]
+    fake = P(1 << 20)  # never dereferenced: every case fails a host check first
+
+    def call(**kw):
+        a = dict(q=fake, qs=None, k=fake, ks=None, w=fake, pos=fake, n=4, L=100, H=4, d=64,
+                 k_top=8, dt=0, idx=fake, sc=None, cap=0, st=None)
+        a.update(kw)
+        return f(a["q"], a["qs"], a["k"], a["ks"], a["w"], a["pos"], a["n"], a["L"], a["H"],
+                 a["d"], a["k_top"], a["dt"], a["idx"], a["sc"], a["cap"], a["st"], None)
+
+    assert call(H=6) == 2 and call(d=48) == 2 and call(k_top=20000) == 2
+    assert call(n=-1) == 1 and call(dt=7) == 1
+    assert call(k=None) == 1 and call(pos=None) == 1 and call(idx=None) == 1
+    assert call(dt=1) == 1  # e4m3 needs scales
+    assert call(cap=4) == 1  # capacity below k
+    assert call(q=P((1 << 20) + 4)) == 5
+    # a problem beyond the 32 MiB array, with null and misaligned pointers:
+    # the pointer errors are reported first
+    big = dict(n=8192, L=1 << 20, H=64, d=128, k_top=2048, dt=1, qs=fake, ks=fake)
+    assert call(**dict(big, pos=None)) == 1
+    assert call(**dict(big, k=P((1 << 20) + 8))) == 5
+    assert call(**big) == 3

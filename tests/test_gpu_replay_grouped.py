@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 import synthetic_inputs as si
+from parity import replay_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -72,8 +73,7 @@ def test_grouped_equals_single(hk, dev, H, d, dt):
     assert st == 0
     ref, bad = oracle.replay(case, idx)
     assert bad == 0
-    scale = np.abs(ref).max(axis=1, keepdims=True)
-    assert (np.abs(sc - ref) <= 1e-3 * np.maximum(np.abs(ref), 1e-2 * scale)).all()
+    assert (np.abs(sc.astype(np.float64) - ref) <= replay_tolerance(case, idx, ref)).all()
 
 
 def test_grouped_exact_integer_data(hk, dev):
@@ -112,7 +112,8 @@ def test_grouped_empty_bad_and_repeated_entries(hk, dev):
     ref, bad = oracle.replay(case, idx)
     assert bad == 2
     ok = (idx >= 0) & (idx < 1000)
-    assert (np.abs(sc[ok] - ref[ok]) <= 1e-3 * np.maximum(np.abs(ref[ok]), 1e-3)).all()
+    tol = replay_tolerance(case, idx, ref)
+    assert (np.abs(sc[ok].astype(np.float64) - ref[ok]) <= tol[ok]).all()
 
 
 def test_grouped_k_above_pairing_limit_runs_single(hk, dev):
