@@ -29,7 +29,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int pad_queries(int n) { return (n + kQueryPad - 1) / kQueryPad * kQueryPad; }
 
 struct SelectLayout {
-  size_t perm, qpos, wq, qp, thr, cnt, cand, flist, failed, ctr, rowbuf, rowlist, plan, total;
+  size_t perm, qpos, wq, qp, thr, cnt, cand, flist, failed, ctr, rowbuf, plan, total;
 };
 
 SelectLayout select_layout(int n, int L, int H, int d, int C, hytopk_dtype dt) {
@@ -52,7 +52,6 @@ SelectLayout select_layout(int n, int L, int H, int d, int C, hytopk_dtype dt) {
   s.qp = take(np * H * d * elem_size(dt));
   s.cand = take(np * (size_t)C * 8);
   s.rowbuf = take((size_t)kRecoveryCtas * L * 4);
-  s.rowlist = take((size_t)kRecoveryCtas * L * 8);
   s.plan = take(((size_t)stream_chunks(L) + 1) * 4);
   s.total = off;
   return s;
@@ -165,7 +164,6 @@ hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* 
   ws.failed = base + lay.failed;
   ws.counters = reinterpret_cast<uint32_t*>(base + lay.ctr);
   ws.rowbuf = reinterpret_cast<float*>(base + lay.rowbuf);
-  ws.rowlist = reinterpret_cast<uint64_t*>(base + lay.rowlist);
   ws.plan = reinterpret_cast<int32_t*>(base + lay.plan);
   ws.n_pad = pad_queries(n);
   ws.C = C;
@@ -187,6 +185,23 @@ hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* 
   HYTOPK_TRY(launch_select(p, ws, idx_out, scores_out, stream));
   if ((s = record(opts, HYTOPK_PHASE_RECOVER, stream)) != HYTOPK_OK) return s;
   HYTOPK_TRY(launch_recover(p, ws, idx_out, scores_out, stream));
+  {
+    // Past HYTOPK_MAX_RECOVERY_ROWS failed queries every query is rescored
+    // over its whole context: score-table rows in slot order, written into
+    // the candidate and recovery-row buffers (unused by then) and read back
+    // chunk by chunk. Whether that happens is known only on the device, so
+    // these launches are always made and return at once without a fallback.
+    float* table = reinterpret_cast<float*>(base + lay.cand);
+    const size_t rows_fit = (lay.plan - lay.cand) / ((size_t)L * 4);
+    const int chunk = (int)(rows_fit < (size_t)n ? rows_fit : (size_t)n);
+    FallbackMaps maps;
+    HYTOPK_TRY(prepare_fallback_table(p, ws, &maps));
+    for (int slot0 = 0; chunk > 0 && slot0 < n; slot0 += chunk) {
+      const int rows = n - slot0 < chunk ? n - slot0 : chunk;
+      HYTOPK_TRY(launch_fallback_table(p, ws, maps, slot0, rows, table, stream));
+      HYTOPK_TRY(launch_fallback_topk(p, ws, slot0, rows, table, idx_out, scores_out, stream));
+    }
+  }
   if ((s = record(opts, HYTOPK_NUM_PHASES, stream)) != HYTOPK_OK) return s;
   if (stats_out) HYTOPK_TRY(launch_finalize(ws, n, stats_out, stream));
   return HYTOPK_OK;
@@ -237,10 +252,9 @@ hytopk_status hytopk_replay_grouped(const void* q, const float* q_scale, const v
   return HYTOPK_OK;
 }
 
-// Two-pass workspace: the per-CTA candidate lists of the read-back kernel, the
-// halved folded weights of the queries (padded by one query block), then the
+// Two-pass workspace: the halved folded weights of the queries (padded by one
+// query block), the bf16 copy of e4m3 queries for the mixed type, then the
 // score-table chunk.
-static size_t twopass_lists_bytes(int L) { return align_up((size_t)kTableCtas * L * 8, 1024); }
 static size_t twopass_weights_bytes(int n, int H) {
   return align_up(((size_t)n + kQueryPad) * H * 4, 1024);
 }
@@ -250,7 +264,7 @@ static size_t twopass_qconv_bytes(int n, int H, int d, hytopk_dtype dt) {
   return dt == HYTOPK_E4M3_BF16 ? align_up((size_t)n * H * d * 2, 1024) : 0;
 }
 static size_t twopass_fixed_bytes(int n, int L, int H, int d, hytopk_dtype dt) {
-  return twopass_lists_bytes(L) + twopass_weights_bytes(n, H) + twopass_qconv_bytes(n, H, d, dt);
+  return twopass_weights_bytes(n, H) + twopass_qconv_bytes(n, H, d, dt);
 }
 
 size_t hytopk_twopass_workspace_size(int n, int L, int H, int d, int k_top, hytopk_dtype dt,
@@ -279,14 +293,13 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
   size_t chunk = (workspace_bytes - fixed) / row_bytes;
   if (chunk > (size_t)n) chunk = (size_t)n;
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  uint64_t* lists = reinterpret_cast<uint64_t*>(base);
-  float* hw = reinterpret_cast<float*>(base + twopass_lists_bytes(L));
+  float* hw = reinterpret_cast<float*>(base);
   float* table = reinterpret_cast<float*>(base + fixed);
   const Problem p0 = make_problem(q, q_scale, k, k_scale, w, positions, n, L, H, d, k_top, dt);
   HYTOPK_TRY(launch_fold_weights(p0, n + kQueryPad, hw, stream));  // folds q_scale
   Problem p = p0;
   if (dt == HYTOPK_E4M3_BF16) {
-    void* qconv = base + twopass_lists_bytes(L) + twopass_weights_bytes(n, H);
+    void* qconv = base + twopass_weights_bytes(n, H);
     HYTOPK_TRY(launch_convert_queries(p0, qconv, stream));
     p.q = qconv;
     p.qdt = 0;
@@ -294,8 +307,7 @@ hytopk_status hytopk_select_twopass(const void* q, const float* q_scale, const v
   for (int row0 = 0; row0 < n; row0 += (int)chunk) {
     const int rows = (int)((size_t)(n - row0) < chunk ? (size_t)(n - row0) : chunk);
     HYTOPK_TRY(launch_table(p, row0, rows, table, hw, dev_status, stream));
-    HYTOPK_TRY(launch_table_topk(p, row0, rows, table, lists, kTableCtas, idx_out, scores_out,
-                                 stream));
+    HYTOPK_TRY(launch_table_topk(p, row0, rows, table, idx_out, scores_out, stream));
   }
   return HYTOPK_OK;
 }

@@ -67,7 +67,6 @@ struct SelectWs {
   uint8_t* failed;      // [n_pad]
   uint32_t* counters;   // [kCtrCount]
   float* rowbuf;        // [kRecoveryCtas, L] full score rows (recovery)
-  uint64_t* rowlist;    // [kRecoveryCtas, L] row candidate lists (recovery)
   int32_t* plan;        // [nchunks + 1] filter work items per key chunk
   int n_pad, C;
 };

@@ -101,7 +101,6 @@ struct GArgs {
   uint32_t* counters;
   const int32_t* failed_list;
   float* rowbuf;
-  uint64_t* rowlist;
   int32_t* idx_out;
   float* scores_out;
   // layout
@@ -316,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       MODE == kThreshold ? a.n_pad : (MODE == kReplay ? a.n : (PAIR ? (a.n + 1) / 2 : 0));
   const uint32_t n_failed = MODE == kRecover ? a.counters[kCtrFailed] : 0u;
   const bool fallback = n_failed > HYTOPK_MAX_RECOVERY_ROWS;
-  const int n_rec = MODE == kRecover ? (fallback ? a.n_pad : (int)n_failed) : 0;
+  // past the limit every query goes through the table path of the fallback instead
+  const int n_rec = MODE == kRecover ? (fallback ? 0 : (int)n_failed) : 0;
 
   for (int it = blockIdx.x;; it += gridDim.x) {
     // ---- pick the query (uniform across the CTA) ----
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       t = 2 * item;
       tB = t + 1 < a.n ? t + 1 : -1;
     } else {
-      slot = MODE == kThreshold ? item : (fallback ? item : a.failed_list[item]);
+      slot = MODE == kThreshold ? item : a.failed_list[item];
       t = a.perm[slot];
       ctx = a.qpos[slot] + 1;
       if (t < 0) continue;
@@ -668,8 +668,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       if (threadIdx.x == 0) a.thr[slot] = desc32_score(v);
       __syncthreads();
     } else if (MODE == kRecover) {
-      const int got = cta_row_topk(a.rowbuf + (size_t)blockIdx.x * a.L, ctx, a.k_top,
-                                   a.rowlist + (size_t)blockIdx.x * a.L, sel, rsc);
+      const int got = cta_row_topk(a.rowbuf + (size_t)blockIdx.x * a.L, ctx, a.k_top, sel, rsc);
       write_selection(sel, got, a.k_top, a.idx_out + (size_t)t * a.k_top,
                       a.scores_out ? a.scores_out + (size_t)t * a.k_top : nullptr);
       __syncthreads();

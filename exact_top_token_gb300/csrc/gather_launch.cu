@@ -54,7 +54,6 @@ void slot_args(gather::GArgs& a, const SelectWs& ws) {
   a.counters = ws.counters;
   a.failed_list = ws.failed_list;
   a.rowbuf = ws.rowbuf;
-  a.rowlist = ws.rowlist;
   a.status = ws.counters + kCtrStatus;
 }
 

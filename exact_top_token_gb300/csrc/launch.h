@@ -36,8 +36,20 @@ cudaError_t launch_select(const Problem& p, const SelectWs& ws, int32_t* idx_out
                           float* scores_out, cudaStream_t st);
 cudaError_t launch_finalize(const SelectWs& ws, int n, hytopk_stats* stats, cudaStream_t st);
 cudaError_t launch_table_topk(const Problem& p, int row0, int rows, const float* table,
-                              uint64_t* lists, int n_lists, int32_t* idx_out, float* scores_out,
-                              cudaStream_t st);
+                              int32_t* idx_out, float* scores_out, cudaStream_t st);
+// The fallback of hytopk_select past HYTOPK_MAX_RECOVERY_ROWS failed queries:
+// slots slot0 .. slot0 + rows - 1 scored into a table (slot order, one row of
+// L scores each) and their exact top-k read back. Both launches do nothing
+// unless the failed-query counter exceeds the limit.
+struct FallbackMaps {
+  CUtensorMap km, qm;  // keys; slot-packed queries
+};
+cudaError_t prepare_fallback_table(const Problem& p, const SelectWs& ws, FallbackMaps* m);
+cudaError_t launch_fallback_table(const Problem& p, const SelectWs& ws, const FallbackMaps& m,
+                                  int slot0, int rows, float* table, cudaStream_t st);
+cudaError_t launch_fallback_topk(const Problem& p, const SelectWs& ws, int slot0, int rows,
+                                 const float* table, int32_t* idx_out, float* scores_out,
+                                 cudaStream_t st);
 
 // tmap.cu
 bool make_tmap_2d(CUtensorMap* map, const void* base, int dt, uint64_t inner_elems, uint64_t rows,

@@ -323,6 +323,120 @@ static __device__ void cta_sort_u64(uint64_t* sel, int n, RadixScratch& sc) {
   __syncthreads();
 }
 
+// Selection and order in one bucket pass, for lists of at most PER * blockDim.x
+// unique keys held in registers (a query's candidates in the common case).
+// The keys are read once; their upper 32 bits (the score part) less the
+// minimum, shifted right until the range fits 4096 ordered buckets, give each
+// key a bucket; the buckets are counted and prefix-summed, which locates the
+// bucket b* holding the k_sel-th smallest key. Keys of buckets up to b* are
+// scattered by bucket into tmp, and each one's final place is its bucket's
+// start plus the number of the bucket's keys below it; the places below k_sel
+// are written to sel. The result is the k_sel smallest keys in ascending order
+// in sel[0 .. k_sel) -- the radix select and sort of the list. Returns false,
+// leaving sel untouched, when the list is longer than PER * blockDim.x or a
+// bucket holds more than kMaxBucket keys (many equal scores); the caller then
+// takes the general path. tmp needs room for k_sel + kMaxBucket keys.
+constexpr uint32_t kMaxBucket = 32;
+
+// key[r] holds list entry threadIdx.x + r * blockDim.x (loaded by the caller,
+// who may read past cnt: entries at or past cnt are ignored).
+template <int PER>
+static __device__ bool cta_select_sort_regs(uint64_t (&key)[PER], int cnt, int k_sel,
+                                            uint64_t* sel, uint64_t* tmp, RadixScratch& sc) {
+  constexpr int NB = 4096;
+  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (cnt > PER * T) return false;
+  if (k_sel <= 0) return true;
+  if (tid == 0) {
+    sc.out[0] = 0xffffffffu;
+    sc.out[1] = 0u;
+    sc.out[2] = 0u;
+  }
+  for (int b = tid; b < NB; b += T) sc.hist[b] = 0u;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int i = tid + r * T;
+    if (i < cnt) {
+      const uint32_t u = (uint32_t)(key[r] >> 32);
+      lo = min(lo, u);
+      hi = max(hi, u);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  __syncthreads();  // out[] and hist cleared
+  if (lane == 0) {
+    atomicMin(&sc.out[0], lo);
+    atomicMax(&sc.out[1], hi);
+  }
+  __syncthreads();
+  const uint32_t kmin = sc.out[0], range = sc.out[1] - kmin;
+  const int width = range == 0u ? 0 : 32 - __clz(range);
+  const int sh = width > 12 ? width - 12 : 0;
+  auto bucket = [&](uint64_t k) { return (((uint32_t)(k >> 32)) - kmin) >> sh; };
+#pragma unroll
+  for (int r = 0; r < PER; ++r)
+    if (tid + r * T < cnt) atomicAdd(&sc.hist[bucket(key[r])], 1u);
+  __syncthreads();
+  // exclusive prefix sum; the bucket where the running count reaches k_sel;
+  // the largest bucket
+  const int per = (NB + T - 1) / T, b0 = tid * per, b1 = min(b0 + per, NB);
+  uint32_t local = 0, big = 0;
+  for (int b = b0; b < b1; ++b) {
+    const uint32_t c = sc.hist[b];
+    local += c;
+    big = max(big, c);
+  }
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+    big = max(big, __shfl_xor_sync(0xffffffffu, big, o));
+  }
+  if (lane == 31) sc.warp_sums[warp] = incl;
+  if (lane == 0) atomicMax(&sc.out[2], big);
+  __syncthreads();
+  uint32_t run = incl - local;
+  for (int w = 0; w < warp; ++w) run += sc.warp_sums[w];
+  for (int b = b0; b < b1; ++b) {
+    const uint32_t c = sc.hist[b];
+    if (run < (uint32_t)k_sel && (uint32_t)k_sel <= run + c) sc.out[3] = (uint32_t)b;
+    sc.hist[b] = run;
+    run += c;
+  }
+  const bool crowded = sc.out[2] > kMaxBucket;
+  __syncthreads();  // hist[b] = start of bucket b; out[3] = b*
+  if (crowded) return false;
+  const uint32_t bstar = sc.out[3];
+  uint32_t mine = 0;  // bit r: key r is scattered
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const uint32_t b = bucket(key[r]);
+    if (tid + r * T < cnt && b <= bstar) {
+      tmp[atomicAdd(&sc.hist[b], 1u)] = key[r];
+      mine |= 1u << r;
+    }
+  }
+  __syncthreads();  // hist[b] = end of bucket b (for b <= b*)
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    if (mine & (1u << r)) {
+      const uint32_t b = bucket(key[r]);
+      const uint32_t start = b > 0 ? sc.hist[b - 1] : 0u, end = sc.hist[b];
+      uint32_t dst = start;
+      for (uint32_t j = start; j < end; ++j) dst += tmp[j] < key[r] ? 1u : 0u;
+      if (dst < (uint32_t)k_sel) sel[dst] = key[r];
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
 // Write one query's sorted selection: k_eff keys then padding to k_top.
 __device__ __forceinline__ void write_selection(const uint64_t* sel, int k_eff, int k_top,
                                                 int32_t* idx_row, float* score_row) {
@@ -338,72 +452,168 @@ __device__ __forceinline__ void write_selection(const uint64_t* sel, int k_eff, 
   }
 }
 
-// Exact top-k of a full score row[0..ctx): a 12-bit histogram of desc32 finds
-// the bin holding the k-th best score, the keys in and above that bin are
-// listed (list: ctx entries of global scratch), and the list is radix
-// selected and sorted. Result: sel[0..min(k,ctx)) sorted.
-static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_t* list, uint64_t* sel,
-                            RadixScratch& sc) {
+// Four consecutive scores of a row starting at position s (s + 3 < ctx), read
+// with one 16-byte load when the row is 16-byte aligned.
+__device__ __forceinline__ float4 load4(const float* row, bool vec, int s) {
+  if (vec) return *reinterpret_cast<const float4*>(row + s);
+  return make_float4(row[s], row[s + 1], row[s + 2], row[s + 3]);
+}
+
+// Exact top-k of a full score row[0..ctx). A 12-bit histogram of desc32
+// (one pass over the row) finds the bin holding the k-th best score. When the
+// keys in and above that bin fit `list` (shared memory, `cap` keys; may be
+// null), a second pass lists them there and they are radix selected and
+// sorted in shared memory. Otherwise the radix select goes on over the row:
+// further digits of 12 and 8 bits (one pass each, restricted to the keys under
+// the prefix found so far; a pass that ends with a bin whose keys are all
+// needed stops early) find the k-th best score, and a last pass keeps every
+// score before it and, among the scores tied with it, the lowest positions
+// (counted in position order across the CTA). Result: sel[0..min(k, ctx))
+// sorted.
+static __device__ int cta_row_topk(const float* row, int ctx, int k_top, uint64_t* sel,
+                                   RadixScratch& sc, uint64_t* list = nullptr, int cap = 0) {
   const int k_eff = ctx < k_top ? ctx : k_top;
   if (k_eff <= 0) return 0;
-  for (int b = threadIdx.x; b < 4096; b += blockDim.x) sc.hist[b] = 0;
-  __syncthreads();
-  // rows that start on a 16-byte boundary are read four scores per load
-  // (positions 4i .. 4i+3 by thread i mod blockDim), the rest one per load
+  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-  const int nvec = vec ? ctx / 4 : 0;
-  const float4* row4 = reinterpret_cast<const float4*>(row);
-  for (int i0 = 0; i0 < nvec; i0 += blockDim.x) {
-    const int i = i0 + threadIdx.x;
-    const bool in = i < nvec;
-    const float4 v = in ? row4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    hist_add(sc.hist, desc32(v.x) >> 20, in);
-    hist_add(sc.hist, desc32(v.y) >> 20, in);
-    hist_add(sc.hist, desc32(v.z) >> 20, in);
-    hist_add(sc.hist, desc32(v.w) >> 20, in);
-  }
-  for (int s0 = 4 * nvec; s0 < ctx; s0 += blockDim.x) {
-    const int s = s0 + threadIdx.x;
-    hist_add(sc.hist, s < ctx ? desc32(row[s]) >> 20 : 0u, s < ctx);
-  }
-  __syncthreads();
-  cta_find_crossing(sc.hist, 4096, (uint32_t)k_eff, sc.warp_sums, sc.out);
-  const uint32_t bin = sc.out[0];
-  if (threadIdx.x == 0) sc.counter = 0;
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  // list (score, position) of every score in or above the crossing bin
-  auto list_if = [&](float v, int s, bool in) {
-    const bool take = in && (desc32(v) >> 20) <= bin;
+  const int n4 = ctx / 4;  // whole groups of four positions; the rest one by one
+  // one pass over the row: f(score, position, in range) for every position,
+  // four groups of four in flight per thread
+  auto sweep = [&](auto&& f) {
+    constexpr int U = 4;
+    for (int i0 = 0; i0 < n4; i0 += U * T) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * T + tid;
+        v[u] = i < n4 ? load4(row, vec, 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * T + tid;
+        const bool in = i < n4;
+        f(v[u].x, 4 * i, in);
+        f(v[u].y, 4 * i + 1, in);
+        f(v[u].z, 4 * i + 2, in);
+        f(v[u].w, 4 * i + 3, in);
+      }
+    }
+    for (int s0 = 4 * n4; s0 < ctx; s0 += T) {
+      const int s = s0 + tid;
+      f(s < ctx ? row[s] : 0.0f, s, s < ctx);
+    }
+  };
+  // warp-aggregated append of the keys for which take holds
+  auto append = [&](uint64_t* dst, float v, int s, bool take) {
     const unsigned mask = __ballot_sync(0xffffffffu, take);
     if (mask) {
       const int leader = __ffs(mask) - 1;
       uint32_t base = 0;
       if (lane == leader) base = atomicAdd(&sc.counter, (uint32_t)__popc(mask));
       base = __shfl_sync(0xffffffffu, base, leader);
-      if (take) list[base + __popc(mask & ((1u << lane) - 1u))] = cand_key(v, s);
+      if (take) dst[base + __popc(mask & ((1u << lane) - 1u))] = cand_key(v, s);
     }
   };
-  for (int i0 = 0; i0 < nvec; i0 += blockDim.x) {
-    const int i = i0 + threadIdx.x;
-    const bool in = i < nvec;
-    const float4 v = in ? row4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-    list_if(v.x, 4 * i, in);
-    list_if(v.y, 4 * i + 1, in);
-    list_if(v.z, 4 * i + 2, in);
-    list_if(v.w, 4 * i + 3, in);
+  uint32_t prefix = 0, need = (uint32_t)k_eff;
+  int done = 0;
+  bool whole = false;  // every key under the final prefix is kept
+  for (int p = 0; p < 3 && !whole; ++p) {
+    const int bits = p == 2 ? 8 : 12, shift = 32 - done - bits, nb = 1 << bits;
+    for (int b = tid; b < nb; b += T) sc.hist[b] = 0;
+    __syncthreads();
+    sweep([&](float v, int, bool in) {
+      const uint32_t d = desc32(v);
+      in = in && (done == 0 || (d >> (32 - done)) == prefix);
+      hist_add(sc.hist, (d >> shift) & (uint32_t)(nb - 1), in);
+    });
+    __syncthreads();
+    cta_find_crossing(sc.hist, nb, need, sc.warp_sums, sc.out);
+    const uint32_t bin = sc.out[0], before = sc.out[1];
+    const uint32_t in_bin = sc.hist[bin];
+    if (p == 0 && list != nullptr && (uint64_t)before + in_bin <= (uint64_t)cap) {
+      // the keys in and above the bin fit the shared-memory list
+      if (tid == 0) sc.counter = 0;
+      __syncthreads();
+      sweep([&](float v, int s, bool in) { append(list, v, s, in && (desc32(v) >> 20) <= bin); });
+      __syncthreads();
+      const int listed = (int)sc.counter;
+      __syncthreads();
+      const int got = cta_select_smallest_u64(list, listed, k_eff, sel, sc);
+      cta_sort_u64(sel, got, sc);
+      return got;
+    }
+    need -= before;
+    prefix = (prefix << bits) | bin;
+    done += bits;
+    whole = in_bin == need;
+    __syncthreads();
   }
-  for (int s0 = 4 * nvec; s0 < ctx; s0 += blockDim.x) {
-    const int s = s0 + threadIdx.x;
-    const bool in = s < ctx;
-    list_if(in ? row[s] : 0.0f, s, in);
+  // Keep: desc32 >> (32 - done) below the prefix (all of them), and under the
+  // prefix either all (whole) or, tied at the k-th score (done == 32), the
+  // `need` lowest positions.
+  const int drop = 32 - done;
+  if (tid == 0) {
+    sc.counter = 0;
+    sc.out[2] = 0;  // tied keys seen so far
   }
   __syncthreads();
-  const int listed = (int)sc.counter;
-  __syncthreads();
-  const int got = cta_select_smallest_u64(list, listed, k_eff, sel, sc);
-  cta_sort_u64(sel, got, sc);
-  return got;
+  if (whole) {
+    sweep([&](float v, int s, bool in) {
+      const uint32_t hi = desc32(v) >> drop;
+      append(sel, v, s, in && hi <= prefix);
+    });
+    __syncthreads();
+  } else {
+    // positions in order, T*4 at a time, so that the tied keys are ranked by
+    // position with one CTA scan per group
+    const int groups = (ctx + 4 * T - 1) / (4 * T);
+    for (int gi = 0; gi < groups; ++gi) {
+      const int s = gi * 4 * T + 4 * tid;
+      float v[4];
+      bool in[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) in[j] = s + j < ctx;
+      if (s + 3 < ctx) {
+        const float4 f = load4(row, vec, s);
+        v[0] = f.x;
+        v[1] = f.y;
+        v[2] = f.z;
+        v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = in[j] ? row[s + j] : 0.0f;
+      }
+      // rank of this thread's first tied key: tied keys of earlier groups, of
+      // earlier warps, of earlier lanes
+      uint32_t ties = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ties += (in[j] && desc32(v[j]) == prefix) ? 1u : 0u;
+      uint32_t incl = ties;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      if (lane == 31) sc.warp_sums[warp] = incl;
+      __syncthreads();
+      uint32_t rank = sc.out[2] + incl - ties;
+      for (int w = 0; w < warp; ++w) rank += sc.warp_sums[w];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t d = desc32(v[j]);
+        const bool tie = in[j] && d == prefix;
+        append(sel, v[j], s + j, in[j] && (d < prefix || (tie && rank < need)));
+        rank += tie ? 1u : 0u;
+      }
+      __syncthreads();
+      if (tid == T - 1) sc.out[2] = rank;  // the last thread's running rank
+      const bool full = sc.counter >= (uint32_t)k_eff;
+      __syncthreads();
+      if (full) break;
+    }
+  }
+  cta_sort_u64(sel, k_eff, sc);
+  return k_eff;
 }
 
 }  // namespace hytopk

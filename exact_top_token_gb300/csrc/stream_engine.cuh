@@ -59,16 +59,22 @@ struct Cfg {
   static constexpr int KT_BYTES = 128 * RB;
   static constexpr int QG_BYTES = 256 * RB;
   static constexpr int STAGES = RB == 256 ? 4 : (RB == 128 ? 6 : 8);
+  // q operand buffers (a second buffer, loading the next item's q rows during
+  // this item, measured slower at 1M keys: kept at one)
+  static constexpr int QBUF = 1;
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + NG * QG_BYTES;
+  static constexpr int K_OFF = Q_OFF + QBUF * NG * QG_BYTES;
   static constexpr int BAR_OFF = K_OFF + STAGES * KT_BYTES;
-  static constexpr int NBARS = 2 * STAGES + 4 + 2 + 8;   // + item ring full / empty [4]
+  static constexpr int NBARS = 2 * STAGES + 4 + 4 + 8;   // + q full / empty [2], item ring [4]
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;      // tmem base, abort flag, item ring
   static constexpr int POS_OFF = MISC_OFF + 32;
   static constexpr int THR_OFF = POS_OFF + QB * 4;
   static constexpr int ROW_OFF = THR_OFF + QB * 4;
   // per-item candidate staging (filter): CAP entries per query slot of the block
-  static constexpr int STAGE_CAP = (1024 / QB) > 8 ? (1024 / QB) : 8;
+  // (for 16 <= H <= 32, whose warps stage into private regions of
+  // STAGE_CAP / 4 entries flushed when full, at least 32 entries a region)
+  static constexpr int STAGE_CAP_MIN = (H >= 16 && H <= 32) ? 128 : 8;
+  static constexpr int STAGE_CAP = (1024 / QB) > STAGE_CAP_MIN ? (1024 / QB) : STAGE_CAP_MIN;
   static constexpr int SCNT_OFF = ROW_OFF + QB * 4;
   static constexpr int STAGE_OFF = ((SCNT_OFF + QB * 4) + 15) / 16 * 16;
   static constexpr int END = STAGE_OFF + (MODE_STAGING ? QB * STAGE_CAP * 8 : 0);
@@ -109,6 +115,10 @@ struct Args {
   // MODE 0: global item counter (zeroed before the launch); null: items are
   // dealt round robin (MODE 1, whose items cost the same)
   uint32_t* work;
+  // MODE 1 inside hytopk_select (the fallback past HYTOPK_MAX_RECOVERY_ROWS
+  // failed queries): the failed-query counter; the launch does nothing unless
+  // it exceeds that limit. Null: always run.
+  const uint32_t* gate;
 };
 
 __device__ __forceinline__ int find_chunk(const int32_t* off, int nchunks, int item) {
@@ -279,28 +289,9 @@ __device__ __forceinline__ void flush_staged(int block, uint32_t* scnt, const ui
 }
 
 // Private staging, for warps that serve at most a few queries of the block:
-// the (query, lane quadrant) pair owns a region of CAP / 4 entries and the warp
-// keeps its fill level in a register, so an append needs no atomic at all.
-template <int CAP4>
-__device__ __forceinline__ void append_private(bool pass, float score, int s, int region, int slot,
-                                               uint32_t& fill, uint64_t* stage, int32_t* cnt,
-                                               uint64_t* cand, int C) {
-  const unsigned mask = __ballot_sync(0xffffffffu, pass);
-  if (mask == 0u) return;
-  const int lane = threadIdx.x & 31;
-  if (pass) {
-    const uint32_t at = fill + (uint32_t)__popc(mask & ((1u << lane) - 1u));
-    const uint64_t key = cand_key(score, s);
-    if (at < (uint32_t)CAP4) {
-      stage[region * CAP4 + at] = key;
-    } else {
-      const int g = atomicAdd(cnt + slot, 1);
-      if (g < C) cand[(size_t)slot * C + g] = key;
-    }
-  }
-  fill += (uint32_t)__popc(mask);
-}
-
+// the (query, lane quadrant) pair owns a region of CAP4 entries and the warp
+// keeps its fill level in a register, so an append needs no atomic.
+//
 // Move one private region to the query's global buffer (one atomic) and
 // empty it; the whole warp calls it.
 template <int CAP4>
@@ -320,6 +311,40 @@ __device__ __forceinline__ void flush_private(int region, int slot, uint32_t& fi
     if (g < C) cand[(size_t)slot * C + g] = stage[region * CAP4 + i];
   }
   __syncwarp();
+}
+
+// Append (score, key) for the lanes where pass holds; the whole warp calls
+// it. FLUSH_FULL (used with H <= 32, whose short-context queries can pass
+// most keys): a region that cannot take this ballot's keys is flushed first,
+// one atomic for the region (CAP4 >= 32). Otherwise (H = 64, a few dozen
+// candidates per query and item) keys past the region go to the global buffer
+// one atomic each; that branch-light form measured faster there.
+template <int CAP4, bool FLUSH_FULL>
+__device__ __forceinline__ void append_private(bool pass, float score, int s, int region, int slot,
+                                               uint32_t& fill, uint64_t* stage, int32_t* cnt,
+                                               uint64_t* cand, int C) {
+  const unsigned mask = __ballot_sync(0xffffffffu, pass);
+  if (mask == 0u) return;
+  const int lane = threadIdx.x & 31;
+  if constexpr (FLUSH_FULL) {
+    static_assert(CAP4 >= 32, "a region must take one ballot's keys");
+    const uint32_t np = (uint32_t)__popc(mask);
+    if (fill + np > (uint32_t)CAP4) flush_private<CAP4>(region, slot, fill, stage, cnt, cand, C);
+    if (pass) stage[region * CAP4 + fill + __popc(mask & ((1u << lane) - 1u))] = cand_key(score, s);
+    fill += np;
+  } else {
+    if (pass) {
+      const uint32_t at = fill + (uint32_t)__popc(mask & ((1u << lane) - 1u));
+      const uint64_t key = cand_key(score, s);
+      if (at < (uint32_t)CAP4) {
+        stage[region * CAP4 + at] = key;
+      } else {
+        const int g = atomicAdd(cnt + slot, 1);
+        if (g < C) cand[(size_t)slot * C + g] = key;
+      }
+    }
+    fill += (uint32_t)__popc(mask);
+  }
 }
 
 template <int D, int DT, int H, int MODE>
@@ -351,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = bars + STAGES;
   uint64_t* acc_full = bars + 2 * STAGES;       // [2]
   uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2]
-  uint64_t* q_full = bars + 2 * STAGES + 4;
-  uint64_t* q_empty = bars + 2 * STAGES + 5;
-  uint64_t* item_full = bars + 2 * STAGES + 6;    // [4]
-  uint64_t* item_empty = bars + 2 * STAGES + 10;  // [4]
+  uint64_t* q_full = bars + 2 * STAGES + 4;       // [QBUF]
+  uint64_t* q_empty = bars + 2 * STAGES + 6;      // [QBUF]
+  uint64_t* item_full = bars + 2 * STAGES + 8;    // [4]
+  uint64_t* item_empty = bars + 2 * STAGES + 12;  // [4]
   volatile int32_t* item_ring = reinterpret_cast<volatile int32_t*>(smem + C_::MISC_OFF + 16);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C_::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C_::MISC_OFF + 4);
@@ -365,6 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* stage_s = reinterpret_cast<uint64_t*>(smem + C_::STAGE_OFF);
   constexpr int CAP = C_::STAGE_CAP;
 
+  if (MODE == 1 && a.gate != nullptr &&
+      *reinterpret_cast<const volatile uint32_t*>(a.gate) <= HYTOPK_MAX_RECOVERY_ROWS)
+    return;  // uniform over the grid, before any barrier or TMEM is set up
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nchunks = (a.L + kChunkKeys - 1) / kChunkKeys;
   const int nblocks = MODE == 0 ? a.n_pad / QB : (a.rows + QB - 1) / QB;
@@ -379,8 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(acc_full + i, 1);
       tc::mbar_init(acc_empty + i, C_::ACTIVE_EPI);
     }
-    tc::mbar_init(q_full, 1);
-    tc::mbar_init(q_empty, 1);
+    for (int i = 0; i < C_::QBUF; ++i) {
+      tc::mbar_init(q_full + i, 1);
+      tc::mbar_init(q_empty + i, 1);
+    }
     for (int i = 0; i < 4; ++i) {
       tc::mbar_init(item_full + i, 1);
       tc::mbar_init(item_empty + i, 1 + kEpiWarps);
@@ -429,22 +459,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_prefetch(&kmap);
         tc::tma_prefetch(&qmap);
         int stage = 0;
-        uint32_t sphase = 0, qphase = 0;
+        uint32_t sphase = 0;
         uint32_t pending = 0, pend_phase = 0, q_loads = 0;  // issued loads, for a clean abort
         for (int n = 0;; ++n) {
           const int i = publish_item(n);
           if (i < 0 || i >= total) break;
           const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
-          if (!tc::mbar_wait(q_empty, qphase ^ 1u, abort_flag, a.status)) break;
-          qphase ^= 1u;
-          tc::mbar_expect_tx(q_full, NG * C_::QG_BYTES);
+          // q buffer of the n-th item: n % QBUF, its (n / QBUF)-th use
+          const int qb = n % C_::QBUF;
+          const uint32_t qpar = (uint32_t)(n / C_::QBUF) & 1u;
+          if (!tc::mbar_wait(q_empty + qb, qpar ^ 1u, abort_flag, a.status)) break;
+          tc::mbar_expect_tx(q_full + qb, NG * C_::QG_BYTES);
           const int qrow0 = (MODE == 0 ? itm.block * QB : a.row0 + itm.block * QB) * H;
   #pragma unroll
           for (int g = 0; g < NG; ++g)
   #pragma unroll
             for (int at = 0; at < Geo::kAtoms; ++at)
-              tc::tma_load_2d(smem + C_::Q_OFF + g * C_::QG_BYTES + at * 256 * Geo::kAtom, &qmap,
-                              q_full, at * Geo::kAtom / C_::ES, qrow0 + g * 256);
+              tc::tma_load_2d(smem + C_::Q_OFF + (qb * NG + g) * C_::QG_BYTES +
+                                  at * 256 * Geo::kAtom,
+                              &qmap, q_full + qb, at * Geo::kAtom / C_::ES, qrow0 + g * 256);
           ++q_loads;
           bool ok = true;
           for (int t = 0; t < itm.ntiles; ++t) {
@@ -475,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               while (!tc::mbar_try_wait(k_full + st, (pend_phase >> st) & 1u) &&
                      tc::global_ns() - t0 < 200000000ull) {
               }
-          if (q_loads)
-            while (!tc::mbar_try_wait(q_full, (q_loads - 1) & 1u) &&
+          for (uint32_t j = q_loads > (uint32_t)C_::QBUF ? q_loads - C_::QBUF : 0u; j < q_loads; ++j)
+            while (!tc::mbar_try_wait(q_full + j % C_::QBUF, (j / C_::QBUF) & 1u) &&
                    tc::global_ns() - t0 < 200000000ull) {
             }
         }
@@ -485,17 +518,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // ---------------- MMA issuer ----------------
         constexpr uint32_t IDESC = tc::instr_desc(DT, 128, 256);
-        const uint32_t q_addr = tc::smem_u32(smem + C_::Q_OFF);
-        const uint32_t k_addr = tc::smem_u32(smem + C_::K_OFF);
+        // Descriptors of stage 0, K-step 0. The start address field (bits
+        // 0-13, address / 16) is the only part that differs between stages
+        // and K-steps, and shared-memory addresses stay below 256 KB, so a
+        // descriptor is its template plus (byte offset / 16) in the low word.
+        const uint64_t a_tmpl = tc::smem_desc(tc::smem_u32(smem + C_::K_OFF), Geo::kSbo, Geo::kSwizzle);
+        const uint64_t b_tmpl = tc::smem_desc(tc::smem_u32(smem + C_::Q_OFF), Geo::kSbo, Geo::kSwizzle);
+        const uint32_t a_lo = (uint32_t)a_tmpl, a_hi = (uint32_t)(a_tmpl >> 32);
+        const uint32_t b_lo = (uint32_t)b_tmpl, b_hi = (uint32_t)(b_tmpl >> 32);
+        uint32_t a_stage_lo = a_lo;  // a_lo + stage * KT_BYTES / 16
         int stage = 0, acc = 0;
-        uint32_t sphase = 0, aphase = 0, qphase = 0;
+        uint32_t sphase = 0, aphase = 0;
         for (int n = 0;; ++n) {
           const int i = take_item(n);
           if (a.work != nullptr && i >= 0) tc::mbar_arrive(item_empty + (n & 3));
           if (i < 0 || i >= total) break;
           const Item itm = decode<QB, MODE>(a, nchunks, nblocks, item_at(i));
-          if (!tc::mbar_wait(q_full, qphase, abort_flag, a.status)) break;
-          qphase ^= 1u;
+          const int qb = n % C_::QBUF;
+          if (!tc::mbar_wait(q_full + qb, (uint32_t)(n / C_::QBUF) & 1u, abort_flag, a.status))
+            break;
+          const uint32_t bq_lo = b_lo + (uint32_t)((qb * NG * C_::QG_BYTES) >> 4);
           tc::fence_after_sync();
           bool ok = true;
           for (int t = 0; t < itm.ntiles && ok; ++t) {
@@ -514,10 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
   #pragma unroll
               for (int j = 0; j < Geo::kSteps; ++j) {
-                const uint64_t adesc = tc::smem_desc(
-                    k_addr + stage * C_::KT_BYTES + Geo::step_offset(j, 128), Geo::kSbo, Geo::kSwizzle);
-                const uint64_t bdesc = tc::smem_desc(
-                    q_addr + g * C_::QG_BYTES + Geo::step_offset(j, 256), Geo::kSbo, Geo::kSwizzle);
+                const uint64_t adesc =
+                    tc::desc_from_words(a_stage_lo + (Geo::step_offset(j, 128) >> 4), a_hi);
+                const uint64_t bdesc = tc::desc_from_words(
+                    bq_lo + ((g * C_::QG_BYTES + Geo::step_offset(j, 256)) >> 4), b_hi);
                 tc::mma<DT>(d_tmem, adesc, bdesc, IDESC, j > 0 ? 1u : 0u);
               }
               tc::mma_commit(acc_full + acc);
@@ -525,12 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (acc == 0) aphase ^= 1u;
             }
             tc::mma_commit(k_empty + stage);
+            a_stage_lo += C_::KT_BYTES >> 4;
             if (++stage == STAGES) {
               stage = 0;
+              a_stage_lo = a_lo;
               sphase ^= 1u;
             }
           }
-          tc::mma_commit(q_empty);
+          tc::mma_commit(q_empty + qb);
           if (!ok) break;
         }
       }
@@ -631,21 +675,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool ok = true;
       const int s_first = itm.tile0 * kTileKeys + quad * 32 + lane;
-      float ks_next = DT == 1 ? (s_first < a.L ? __ldg(a.k_scale + s_first) : 0.0f) : 1.0f;
+      // key scales are read one tile ahead from an index clamped to L - 1: a
+      // key at or past L (zero-filled by the tile load) fails the causal test
+      // whatever its scale, and the clamped read stays inside k_scale
+      const int s_last = a.L - 1;
+      float ks_next = DT == 1 ? __ldg(a.k_scale + min(s_first, s_last)) : 1.0f;
+      // TMEM address of this warp's lane quadrant and column span in
+      // accumulator 0; accumulator 1 is 256 columns on
+      const uint32_t tbase0 =
+          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(sub * CW);
       for (int t = 0; t < itm.ntiles && ok; ++t) {
-        const int s = (itm.tile0 + t) * kTileKeys + quad * 32 + lane;
+        const int s = s_first + t * kTileKeys;
         const float ks = ks_next;
-        if (DT == 1) {
-          const int sn = s + kTileKeys;
-          ks_next = (t + 1 < itm.ntiles && sn < a.L) ? __ldg(a.k_scale + sn) : 0.0f;
-        }
+        if (DT == 1) ks_next = __ldg(a.k_scale + min(s + kTileKeys, s_last));
         if (!tc::mbar_wait(acc_full + acc, aphase, abort_flag, a.status)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t tbase =
-            tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 256 + sub * CW);
+        const uint32_t tbase = tbase0 + ((uint32_t)acc << 8);
         HeadSum<H> hs;
         if (!REG_W) hs.reset();
         float va[KC];
@@ -684,7 +732,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sc = hs.total();
                 if (!REG_W) hs.reset();
               }
-              sc = finish_score(sc, ks);
+              // the filter's keys carry the score through cand_key, which
+              // takes -0 as +0, and -0 >= thr exactly when +0 >= thr, so the
+              // filter skips finish_score's zero fixup (same bits kept)
+              sc = MODE == 0 ? sc * ks : finish_score(sc, ks);
               int p;
               float thr;
               if constexpr (REG_META) {
@@ -697,7 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (MODE == 0) {
                 const bool pass = (s <= p) && (sc >= thr);
                 if constexpr (REG_META)
-                  append_private<CAP4>(pass, sc, s, (qlo + qi) * 4 + quad, rrow[qi], fill[qi],
+                  append_private<CAP4, (H <= 32)>(pass, sc, s, (qlo + qi) * 4 + quad, rrow[qi],
+                                                  fill[qi],
                                        stage_s, a.cnt, a.cand, a.C);
                 else
                   append_staged<CAP>(pass, sc, s, qlo + qi, rrow[qi], scnt_s, stage_s, a.cnt,
@@ -710,11 +762,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
-#pragma unroll
-        for (int ch = 0; ch < CW / KC; ++ch) {
-          tc::tmem_ld_n(tbase + ch * KC, va);
+        if constexpr (REG_W) {
+          // two buffers: the load of chunk ch + 1 is in flight while chunk ch
+          // is reduced
+          float vb[KC];
+          constexpr int NCH = CW / KC;
+          tc::tmem_ld_n(tbase, va);
           tc::tmem_wait_ld(va);
-          reduce(va, ch);
+#pragma unroll
+          for (int ch = 0; ch < NCH; ++ch) {
+            if (ch + 1 < NCH) tc::tmem_ld_n(tbase + (ch + 1) * KC, (ch & 1) ? va : vb);
+            reduce((ch & 1) ? vb : va, ch);
+            if (ch + 1 < NCH) tc::tmem_wait_ld((ch & 1) ? va : vb);
+          }
+        } else {
+#pragma unroll
+          for (int ch = 0; ch < CW / KC; ++ch) {
+            tc::tmem_ld_n(tbase + ch * KC, va);
+            tc::tmem_wait_ld(va);
+            reduce(va, ch);
+          }
         }
         tc::fence_before_sync();
         __syncwarp();

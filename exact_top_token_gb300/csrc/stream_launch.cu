@@ -75,6 +75,34 @@ cudaError_t launch_filter(const Problem& p, const SelectWs& ws, int reverse, cud
   return dispatch(p, 0, km, qm, a, num_sms(), st);
 }
 
+cudaError_t prepare_fallback_table(const Problem& p, const SelectWs& ws, FallbackMaps* m) {
+  const int es = p.dt == 0 ? 2 : 1;
+  if (!key_map(p, &m->km)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&m->qm, ws.qp, p.dt, (uint64_t)p.d, (uint64_t)ws.n_pad * p.H,
+                    atom_bytes(p) / es, 256, atom_bytes(p)))
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+cudaError_t launch_fallback_table(const Problem& p, const SelectWs& ws, const FallbackMaps& m,
+                                  int slot0, int rows, float* table, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const CUtensorMap& km = m.km;
+  const CUtensorMap& qm = m.qm;
+  stream::Args a{};
+  a.wq = ws.wq;  // halved folded weights in slot order
+  a.positions = ws.qpos;
+  a.table = table;
+  a.row0 = slot0;
+  a.rows = rows;
+  a.n = ws.n_pad;
+  a.k_scale = p.k_scale;
+  a.L = p.L;
+  a.status = ws.counters + kCtrStatus;
+  a.gate = ws.counters + kCtrFailed;
+  return dispatch(p, 1, km, qm, a, num_sms(), st);
+}
+
 cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, const float* hw,
                          uint32_t* status, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;

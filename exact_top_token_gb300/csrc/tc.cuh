@@ -301,6 +301,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo_bytes
   return d;
 }
 
+// A 64-bit descriptor from its two 32-bit words.
+__device__ __forceinline__ uint64_t desc_from_words(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
 // Geometry of a K-major operand tile for rows of RB bytes.
 template <int RB>
 struct Geo {

@@ -118,6 +118,29 @@ def test_recovery_stress_full_fallback(hk, dev):
     assert set(np.flatnonzero(fs["failed"]).tolist()) >= set(case["decoy_rows"].tolist())
 
 
+@pytest.mark.parametrize("dt,kind,mode", [("bf16", "int", "pos_inf"), ("e4m3", "normal", "neg_inf")])
+def test_fallback_table_in_chunks(hk, dev, dt, kind, mode):
+    """More than 64 failed queries with a small candidate buffer: every query
+    is rescored through score-table rows that fill the candidate and
+    recovery-row buffers chunk by chunk (several chunks here)."""
+    import torch
+
+    n, L, k_top = 300, 16384, 64
+    case = si.random_case(L, n, 8, 64, k_top, dt, seed=61, positions="random", kind=kind)
+    thr = torch.full((n,), float("inf") if mode == "pos_inf" else -float("inf"), device=dev)
+    idx, sc, st, t = run_select(hk, case, dev, threshold_override=thr, stats=True,
+                                capacity=k_top)
+    stats = hk.read_stats(st)
+    ctx = case["positions"] + 1
+    assert stats["fallback_used"] == 1 and stats["n_failed"] == int((ctx > k_top).sum()) > 64
+    gi, gs = host(idx, sc)
+    compare(case, np.arange(n), gi, gs, exact=(kind == "int"))
+    # the same selection without the fallback, bit for bit
+    i2, s2, _, _ = run_select(hk, case, dev)
+    assert np.array_equal(i2.cpu().numpy(), gi)
+    assert np.array_equal(s2.cpu().numpy().view(np.uint32), gs.view(np.uint32))
+
+
 # ---- random workloads ---------------------------------------------------------------
 
 @pytest.mark.parametrize("L,n,H,d,k_top,dt,pos", [
