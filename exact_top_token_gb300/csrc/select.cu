@@ -39,7 +39,9 @@ __global__ void k_check(Problem p, SelectWs ws) {
 // at most 16 keys per thread is read once into registers and selected and
 // ordered by one bucket pass (cta_select_sort_regs); longer lists, or lists
 // with crowded buckets (many equal scores), take the radix select over the
-// list in global memory and the general sort. Two CTAs share an SM.
+// list in global memory and the general sort. Two CTAs share an SM. (A
+// persistent form that loads the next slot's candidates while writing this
+// slot's selection measured slower at 1M keys: 0.48 against 0.41 ms.)
 constexpr int kSelectPer = 16;
 constexpr int kSelectThreads = 512;
 
