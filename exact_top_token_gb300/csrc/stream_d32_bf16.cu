@@ -17,6 +17,11 @@ cudaError_t go(const CUtensorMap& km, const CUtensorMap& qm, const stream::Args&
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  if (MODE == 1) {  // the table writer alternates with the read-back: one carveout for both
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+  }
   fn<<<grid, stream::kThreads, smem, st>>>(km, qm, a);
   return cudaGetLastError();
 }
