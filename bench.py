@@ -62,11 +62,12 @@ WORKLOADS = {"glm_1m": si.glm_1m, "glm_1m_adjacent": si.glm_1m_adjacent,
              "recovery_stress": recovery_stress,
              "tiny_exact": si.tiny_exact}
 # DRAM bytes (read + write) of one full-size filter launch, from one ncu
-# capture of the filter kernel at the build named beside it (its launch list is
-# summarised under profiles/). Reported as roofline.traffic only while the
-# running library is that build (the source digest below matches); otherwise
-# the traffic is reported as null.
-FILTER_TRAFFIC = {"glm_1m": {"bytes": 1.0188e9 + 0.3980e9, "build": None}}
+# capture of the filter kernel (dram__bytes_read.sum + dram__bytes_write.sum,
+# a single pass) at the build named beside it by the digest of its source
+# files (profiles/glm_1m_last1024_filter_k_stream_ncu.txt gives the command).
+# Reported as roofline.traffic only while the running library is that build;
+# otherwise the traffic is reported as null.
+FILTER_TRAFFIC = {"glm_1m": {"bytes": 1072620288 + 402857984, "build": "dafdff1ff187"}}
 FILTER_SOURCES = ("stream_engine.cuh", "stream_launch.cu", "stream_d128_e4m3.cu", "tc.cuh",
                   "common.cuh")
 
@@ -345,10 +346,28 @@ def workload_config(case, world=1):
 
 # ---- the GPU arm -------------------------------------------------------------------------
 
-def launches_per_step(dtype):
-    # select: rank, pack, [key-scale check], threshold, plan, filter, check, select,
-    # recover; then one replay launch
-    return (9 if dtype == "e4m3" else 8) + 1
+def fallback_chunks(n, L, k_top, capacity=0):
+    """Score-table chunks of the fallback past 64 failed queries: the candidate
+    buffer and the recovery rows of the select workspace hold whole rows of L
+    scores (the library's workspace layout, 1 KiB-aligned buffers)."""
+    def al(x):
+        return (x + 1023) // 1024 * 1024
+    n_pad = (n + 511) // 512 * 512
+    C = capacity or 8 * k_top
+    rows = (al(n_pad * C * 8) + al(64 * L * 4)) // (L * 4)
+    rows = min(rows, n)
+    return (n + rows - 1) // rows if n else 0
+
+
+def launches_per_step(case):
+    """Kernels of one step: select (rank, pack, [key-scale check], threshold,
+    plan, filter, check, select, recovery, then per fallback chunk the table
+    writer and the read-back, which return at once without a fallback) and
+    one replay launch."""
+    n, H, d = case["q"].shape
+    L = case["k"].shape[0]
+    base = 9 if case["dtype"] == "e4m3" else 8
+    return base + 2 * fallback_chunks(n, L, case["k_top"]) + 1
 
 
 def gpu_arm(args, world, rank, local):
@@ -408,7 +427,7 @@ def gpu_arm(args, world, rank, local):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": case["dtype"], "data": "synthetic", "config": workload_config(case, world),
-            "clocks": clk, "gpu_launches": launches_per_step(case["dtype"]) * args.steps,
+            "clocks": clk, "gpu_launches": launches_per_step(case) * args.steps,
             "roofline": roofline, "select_ms": select_ms, "phases_ms": phase_ms,
             "replay": replay, "peaks": pk}
 
