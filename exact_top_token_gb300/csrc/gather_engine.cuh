@@ -1,20 +1,19 @@
 // gather_engine.cuh -- the tensor-core scoring engine over gathered keys, one
-// query at a time: the sampled threshold of HyTopK, selection replay, and the
-// recovery rescoring of failed queries.
+// query at a time: selection replay and the recovery rescoring of failed
+// queries (the sampled threshold has its own engine, threshold_engine.cuh,
+// dispatched from here).
 //
-// HyScale explainer: the HyTopK paragraph (sample evenly spaced keys of the
-// query's own context, threshold at the sample that stands for about the 3k-th
-// key; small recovery kernels rescore failed queries over their whole
-// context), the worked example (M and r), and the selection-replay paragraph
-// (rescore only the k stored entries).
+// HyScale explainer: the HyTopK paragraph (small recovery kernels rescore
+// failed queries over their whole context) and the selection-replay
+// paragraph (rescore only the k stored entries).
 //
-// Per query: the key rows it needs (samples, stored indices or its whole
-// prefix) are gathered 128 at a time with cp.async into swizzled shared
-// memory; one elected thread multiplies each 128-key tile by the query's
-// H x d operand (tcgen05, N = max(H, 16)); four epilogue warps (TMEM lane =
-// key) reduce the heads with the same arithmetic as the streaming engine.
-// The CTA then finishes the query together: the r-th best sample (threshold),
-// nothing (replay), or an exact top-k of the rescored row (recovery).
+// Per query: the key rows it needs (stored indices or its whole prefix) are
+// gathered 128 at a time with cp.async into swizzled shared memory; one
+// elected thread multiplies each 128-key tile by the query's H x d operand
+// (tcgen05, N = max(H, 16)); four epilogue warps (TMEM lane = key) reduce the
+// heads with the same arithmetic as the streaming engine. The CTA then
+// finishes the query together: nothing (replay) or an exact top-k of the
+// rescored row (recovery).
 //
 // Paired replay (kReplayPair) serves two adjacent queries per item. Adjacent
 // tokens select mostly the same keys (HyScale summary, "What the paper
@@ -32,6 +31,7 @@
 
 #include "radix.cuh"
 #include "stream_engine.cuh"
+#include "threshold_engine.cuh"
 
 namespace hytopk {
 namespace gather {
@@ -276,7 +276,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   int* item_sh = reinterpret_cast<int*>(misc + 2);
   int* ucount = reinterpret_cast<int*>(misc + 3);                // paired: union size
   float* wq_s = reinterpret_cast<float*>(misc + 4);              // [H]
-  uint32_t* keys_s = reinterpret_cast<uint32_t*>(wq_s + 128);    // [kMaxSamples] (threshold)
   RadixScratch& rsc = *reinterpret_cast<RadixScratch*>(ring);    // after the pipeline drains
   uint64_t* sel = reinterpret_cast<uint64_t*>(ring + sizeof(RadixScratch));
   // paired replay, after the ring: the keys of the second query's own rows,
@@ -312,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
   uint32_t p_phase = 0, m_phase = 0, m_aphase = 0, e_aphase = 0;
 
   const int n_items =
-      MODE == kThreshold ? a.n_pad : (MODE == kReplay ? a.n : (PAIR ? (a.n + 1) / 2 : 0));
+      MODE == kReplay ? a.n : (PAIR ? (a.n + 1) / 2 : 0);
   const uint32_t n_failed = MODE == kRecover ? a.counters[kCtrFailed] : 0u;
   const bool fallback = n_failed > HYTOPK_MAX_RECOVERY_ROWS;
   // past the limit every query goes through the table path of the fallback instead
@@ -332,9 +331,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       if (item >= n_items) break;
     }
     if (*abort_flag) break;
-    int slot = -1, t = -1, ctx = 0, nrows = 0, M = 0, r = 0;
+    int slot = -1, t = -1, ctx = 0, nrows = 0;
     int tB = -1;  // paired replay: the second query (t is the first)
-    SampleStep step{};
     if (MODE == kReplay) {
       t = item;
       nrows = a.k_top;
@@ -342,29 +340,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
       t = 2 * item;
       tB = t + 1 < a.n ? t + 1 : -1;
     } else {
-      slot = MODE == kThreshold ? item : a.failed_list[item];
+      slot = a.failed_list[item];
       t = a.perm[slot];
       ctx = a.qpos[slot] + 1;
       if (t < 0) continue;
-      if (MODE == kThreshold) {
-        if (ctx <= a.k_top || a.override_thr) {
-          if (threadIdx.x == 0)
-            a.thr[slot] = ctx <= a.k_top ? -__int_as_float(0x7f800000) : a.override_thr[t];
-          continue;
-        }
-        M = sample_count(ctx);
-        r = threshold_rank(ctx, a.k_top, M);
-        step.init(ctx, M);
-        nrows = M;
-      } else {
-        nrows = ctx;
-      }
+      nrows = ctx;
     }
     // key of row j of this query's list (replay: the stored index, unchecked;
     // paired replay: the union row, always inside [0, L))
     auto key_of = [&](int j) -> int {
       if (j >= nrows) return -1;
-      if (MODE == kThreshold) return step.at(j);
       if (MODE == kReplay) return __ldg(a.idx + (size_t)t * a.k_top + j);
       if (PAIR)
         return j < a.k_top ? __ldg(a.idx + (size_t)t * a.k_top + rja[j]) : xkey[j - a.k_top];
@@ -627,9 +612,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
           e_aphase ^= 1u;
         }
         if (j < nrows) {
-          if (MODE == kThreshold) {
-            keys_s[j] = desc32(sc);
-          } else if (PAIR) {
+          if (PAIR) {
             if (ja >= 0) {
               float v = sc;
               if (!valid) {
@@ -663,11 +646,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
     __syncthreads();
     if (*abort_flag) break;
     // ---- per-query completion (whole CTA) ----
-    if (MODE == kThreshold) {
-      const uint32_t v = cta_kth_smallest_u32(keys_s, M, (uint32_t)r, rsc);
-      if (threadIdx.x == 0) a.thr[slot] = desc32_score(v);
-      __syncthreads();
-    } else if (MODE == kRecover) {
+    if (MODE == kRecover) {
       const int got = cta_row_topk(a.rowbuf + (size_t)blockIdx.x * a.L, ctx, a.k_top, sel, rsc);
       write_selection(sel, got, a.k_top, a.idx_out + (size_t)t * a.k_top,
                       a.scores_out ? a.scores_out + (size_t)t * a.k_top : nullptr);
@@ -683,18 +662,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_gather(const GArgs a) {
 }
 
 // Shared memory of k_gather: q operand + max(stage ring, post-processing
-// scratch) + barriers, weights and (threshold) the sample keys.
+// scratch) + barriers and weights.
 template <int D, int DT, int H, int MODE>
 inline int gather_smem_bytes(int k_top, int* u_bytes) {
   using C_ = Cfg<D, DT, H, MODE>;
   int post = 0;
-  if (MODE == kThreshold) post = (int)sizeof(RadixScratch);
   if (MODE == kRecover) post = (int)sizeof(RadixScratch) + sort_capacity(k_top) * 8;
   int u = C_::RING > post ? C_::RING : post;
   if (MODE == kReplayPair) u = C_::RING + 3 * k_top * 4;  // + xkey, rja, rjb
   u = (u + 15) / 16 * 16;
   *u_bytes = u;
-  const int tail = 8 * C_::NBARS + 16 + 128 * 4 + (MODE == kThreshold ? kMaxSamples * 4 : 0);
+  const int tail = 8 * C_::NBARS + 16 + 128 * 4;
   return 1024 + C_::U_OFF + u + tail;
 }
 
@@ -712,10 +690,28 @@ cudaError_t gather_go(const GArgs& a0, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// The sampled threshold runs on its own engine (threshold_engine.cuh).
+inline thr::TArgs threshold_args(const GArgs& a) {
+  thr::TArgs t{};
+  t.k = a.k;
+  t.k_scale = a.k_scale;
+  t.L = a.L;
+  t.k_top = a.k_top;
+  t.perm = a.perm;
+  t.qpos = a.qpos;
+  t.qp = a.qp;
+  t.wq = a.wq;
+  t.thr = a.thr;
+  t.override_thr = a.override_thr;
+  t.n_pad = a.n_pad;
+  t.status = a.status;
+  return t;
+}
+
 template <int D, int DT, int H>
 cudaError_t gather_modes(int mode, const GArgs& a, int grid, cudaStream_t st) {
   switch (mode) {
-    case kThreshold: return gather_go<D, DT, H, kThreshold>(a, grid, st);
+    case kThreshold: return thr::threshold_go<D, DT, H>(threshold_args(a), grid, st);
     case kReplay: return gather_go<D, DT, H, kReplay>(a, grid, st);
     case kRecover: return gather_go<D, DT, H, kRecover>(a, grid, st);
     case kReplayPair:

@@ -80,49 +80,6 @@ struct alignas(16) RadixScratch {
   uint32_t counter;
 };
 
-// The kk-th smallest (1-based) of keys[0..cnt) (32-bit, duplicates allowed).
-// MSB-first radix select with digits of 12, 12 and 8 bits. When the bin
-// holding the kk-th key holds that key alone, the remaining bits are read
-// from the one key under the prefix instead of further histogram passes (a
-// threshold rank of a few dozen among thousands of samples usually ends
-// after two histograms).
-static __device__ uint32_t cta_kth_smallest_u32(const uint32_t* keys, int cnt, uint32_t kk,
-                                                RadixScratch& sc) {
-  uint32_t prefix = 0;
-  int done = 0;  // resolved high bits
-  for (int p = 0; p < 3; ++p) {
-    const int bits = p == 2 ? 8 : 12, shift = 32 - done - bits, nb = 1 << bits;
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) sc.hist[b] = 0;
-    __syncthreads();
-    for (int e0 = 0; e0 < cnt; e0 += blockDim.x) {
-      const int e = e0 + threadIdx.x;
-      const uint32_t key = e < cnt ? keys[e] : 0u;
-      const bool in = e < cnt && (done == 0 || (key >> (32 - done)) == prefix);
-      hist_add(sc.hist, (key >> shift) & (uint32_t)(nb - 1), in);
-    }
-    __syncthreads();
-    cta_find_crossing(sc.hist, nb, kk, sc.warp_sums, sc.out);
-    const uint32_t bin = sc.out[0], before = sc.out[1];
-    const bool alone = sc.hist[bin] == 1u;
-    kk -= before;
-    prefix = (prefix << bits) | bin;
-    done += bits;
-    __syncthreads();
-    if (alone && done < 32) {
-      // exactly one key carries this prefix: it is the kk-th
-      for (int e = threadIdx.x; e < cnt; e += blockDim.x) {
-        const uint32_t key = keys[e];
-        if ((key >> (32 - done)) == prefix) sc.out[2] = key;
-      }
-      __syncthreads();
-      const uint32_t v = sc.out[2];
-      __syncthreads();
-      return v;
-    }
-  }
-  return prefix;
-}
-
 // Selects the k_sel smallest of the unique keys list[0..cnt) into sel[0..k_sel)
 // (shared memory, unordered). Returns the number written (min(cnt, k_sel)).
 static __device__ int cta_select_smallest_u64(const uint64_t* list, int cnt, int k_sel, uint64_t* sel,
