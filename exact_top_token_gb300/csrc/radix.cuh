@@ -281,25 +281,27 @@ static __device__ void cta_sort_u64(uint64_t* sel, int n, RadixScratch& sc) {
 }
 
 // Selection and order in one bucket pass, for lists of at most PER * blockDim.x
-// unique keys held in registers (a query's candidates in the common case).
-// The keys are read once; their upper 32 bits (the score part) less the
+// unique keys (a query's candidates in the common case). Only the upper 32
+// bits of each key (the score part) are held in registers: hi[r] is that of
+// list entry threadIdx.x + r * blockDim.x (loaded by the caller, who may read
+// past cnt: entries at or past cnt are ignored). The upper halves less their
 // minimum, shifted right until the range fits 4096 ordered buckets, give each
 // key a bucket; the buckets are counted and prefix-summed, which locates the
-// bucket b* holding the k_sel-th smallest key. Keys of buckets up to b* are
-// scattered by bucket into tmp, and each one's final place is its bucket's
-// start plus the number of the bucket's keys below it; the places below k_sel
-// are written to sel. The result is the k_sel smallest keys in ascending order
-// in sel[0 .. k_sel) -- the radix select and sort of the list. Returns false,
-// leaving sel untouched, when the list is longer than PER * blockDim.x or a
-// bucket holds more than kMaxBucket keys (many equal scores); the caller then
-// takes the general path. tmp needs room for k_sel + kMaxBucket keys.
+// bucket b* holding the k_sel-th smallest key. The keys of buckets up to b*
+// are read again whole from the list and scattered by bucket into tmp; each
+// one's final place is its bucket's start plus the number of the bucket's
+// keys below it, and the places below k_sel are written to sel. The result is
+// the k_sel smallest keys in ascending order in sel[0 .. k_sel) -- the radix
+// select and sort of the list. Returns false, leaving sel untouched, when the
+// list is longer than PER * blockDim.x or a bucket holds more than kMaxBucket
+// keys (many equal scores); the caller then takes the general path. tmp needs
+// room for k_sel + kMaxBucket keys.
 constexpr uint32_t kMaxBucket = 32;
 
-// key[r] holds list entry threadIdx.x + r * blockDim.x (loaded by the caller,
-// who may read past cnt: entries at or past cnt are ignored).
 template <int PER>
-static __device__ bool cta_select_sort_regs(uint64_t (&key)[PER], int cnt, int k_sel,
-                                            uint64_t* sel, uint64_t* tmp, RadixScratch& sc) {
+static __device__ bool cta_select_sort_hi(const uint64_t* list, const uint32_t (&hi)[PER], int cnt,
+                                          int k_sel, uint64_t* sel, uint64_t* tmp,
+                                          RadixScratch& sc) {
   constexpr int NB = 4096;
   const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (cnt > PER * T) return false;
@@ -310,34 +312,32 @@ static __device__ bool cta_select_sort_regs(uint64_t (&key)[PER], int cnt, int k
     sc.out[2] = 0u;
   }
   for (int b = tid; b < NB; b += T) sc.hist[b] = 0u;
-  uint32_t lo = 0xffffffffu, hi = 0u;
+  uint32_t lo = 0xffffffffu, top = 0u;
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    const int i = tid + r * T;
-    if (i < cnt) {
-      const uint32_t u = (uint32_t)(key[r] >> 32);
-      lo = min(lo, u);
-      hi = max(hi, u);
+    if (tid + r * T < cnt) {
+      lo = min(lo, hi[r]);
+      top = max(top, hi[r]);
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    top = max(top, __shfl_xor_sync(0xffffffffu, top, o));
   }
   __syncthreads();  // out[] and hist cleared
   if (lane == 0) {
     atomicMin(&sc.out[0], lo);
-    atomicMax(&sc.out[1], hi);
+    atomicMax(&sc.out[1], top);
   }
   __syncthreads();
   const uint32_t kmin = sc.out[0], range = sc.out[1] - kmin;
   const int width = range == 0u ? 0 : 32 - __clz(range);
   const int sh = width > 12 ? width - 12 : 0;
-  auto bucket = [&](uint64_t k) { return (((uint32_t)(k >> 32)) - kmin) >> sh; };
+  auto bucket = [&](uint32_t h) { return (h - kmin) >> sh; };
 #pragma unroll
   for (int r = 0; r < PER; ++r)
-    if (tid + r * T < cnt) atomicAdd(&sc.hist[bucket(key[r])], 1u);
+    if (tid + r * T < cnt) atomicAdd(&sc.hist[bucket(hi[r])], 1u);
   __syncthreads();
   // exclusive prefix sum; the bucket where the running count reaches k_sel;
   // the largest bucket
@@ -370,25 +370,23 @@ static __device__ bool cta_select_sort_regs(uint64_t (&key)[PER], int cnt, int k
   __syncthreads();  // hist[b] = start of bucket b; out[3] = b*
   if (crowded) return false;
   const uint32_t bstar = sc.out[3];
-  uint32_t mine = 0;  // bit r: key r is scattered
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    const uint32_t b = bucket(key[r]);
-    if (tid + r * T < cnt && b <= bstar) {
-      tmp[atomicAdd(&sc.hist[b], 1u)] = key[r];
-      mine |= 1u << r;
+    const int i = tid + r * T;
+    if (i < cnt) {
+      const uint32_t b = bucket(hi[r]);
+      if (b <= bstar) tmp[atomicAdd(&sc.hist[b], 1u)] = __ldg(list + i);
     }
   }
   __syncthreads();  // hist[b] = end of bucket b (for b <= b*)
-#pragma unroll
-  for (int r = 0; r < PER; ++r) {
-    if (mine & (1u << r)) {
-      const uint32_t b = bucket(key[r]);
-      const uint32_t start = b > 0 ? sc.hist[b - 1] : 0u, end = sc.hist[b];
-      uint32_t dst = start;
-      for (uint32_t j = start; j < end; ++j) dst += tmp[j] < key[r] ? 1u : 0u;
-      if (dst < (uint32_t)k_sel) sel[dst] = key[r];
-    }
+  const uint32_t scattered = sc.hist[bstar];
+  for (uint32_t j = tid; j < scattered; j += T) {
+    const uint64_t key = tmp[j];
+    const uint32_t b = bucket((uint32_t)(key >> 32));
+    const uint32_t start = b > 0 ? sc.hist[b - 1] : 0u, end = sc.hist[b];
+    uint32_t dst = start;
+    for (uint32_t m = start; m < end; ++m) dst += tmp[m] < key ? 1u : 0u;
+    if (dst < (uint32_t)k_sel) sel[dst] = key;
   }
   __syncthreads();
   return true;

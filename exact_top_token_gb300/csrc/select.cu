@@ -36,12 +36,11 @@ __global__ void k_check(Problem p, SelectWs ws) {
 }
 
 // One CTA per query slot: select and sort the k best candidates. A list of
-// at most 16 keys per thread is read once into registers and selected and
-// ordered by one bucket pass (cta_select_sort_regs); longer lists, or lists
-// with crowded buckets (many equal scores), take the radix select over the
-// list in global memory and the general sort. Two CTAs share an SM. (A
-// persistent form that loads the next slot's candidates while writing this
-// slot's selection measured slower at 1M keys: 0.48 against 0.41 ms.)
+// at most 16 keys per thread is selected and ordered by one bucket pass
+// (cta_select_sort_hi) with only the keys' upper halves in registers, so that
+// three CTAs share an SM; longer lists, or lists with crowded buckets (many
+// equal scores), take the radix select over the list in global memory and
+// the general sort.
 constexpr int kSelectPer = 16;
 constexpr int kSelectThreads = 512;
 
@@ -53,7 +52,7 @@ __host__ __device__ constexpr int select_tmp_keys(int k_top) {
          (int)kMaxBucket;
 }
 
-__global__ void __launch_bounds__(kSelectThreads, 2) k_select_candidates(Problem p, SelectWs ws,
+__global__ void __launch_bounds__(kSelectThreads, 3) k_select_candidates(Problem p, SelectWs ws,
                                                            int32_t* __restrict__ idx_out,
                                                            float* __restrict__ scores_out) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -61,14 +60,16 @@ __global__ void __launch_bounds__(kSelectThreads, 2) k_select_candidates(Problem
   uint64_t* sel = reinterpret_cast<uint64_t*>(smem_raw + sizeof(RadixScratch));
   uint64_t* tmp = sel + sort_capacity(p.k_top);  // select_tmp_keys(k_top) keys
   const int slot = blockIdx.x;
-  // every read of the slot's state, its first candidates included (the
-  // buffer has C entries whatever the count), is issued before any is used
+  // every read of the slot's state, the upper halves of its first candidates
+  // included (the buffer has C entries whatever the count), is issued before
+  // any is used
   const uint64_t* list = ws.cand + (size_t)slot * ws.C;
-  uint64_t key[kSelectPer];
+  const uint32_t* list_hi = reinterpret_cast<const uint32_t*>(list) + 1;
+  uint32_t hi[kSelectPer];
 #pragma unroll
   for (int r = 0; r < kSelectPer; ++r) {
     const int i = threadIdx.x + r * kSelectThreads;
-    key[r] = i < ws.C ? __ldg(list + i) : ~0ull;
+    hi[r] = i < ws.C ? __ldg(list_hi + 2 * i) : 0xffffffffu;
   }
   const int t = ws.perm[slot];
   const uint32_t n_failed = ws.counters[kCtrFailed];
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(kSelectThreads, 2) k_select_candidates(Problem
   const int cnt = min(ws.cnt[slot], ws.C);
   if (t < 0 || n_failed > HYTOPK_MAX_RECOVERY_ROWS || failed) return;
   const int k_eff = min(p.k_top, cnt);
-  if (!cta_select_sort_regs<kSelectPer>(key, cnt, k_eff, sel, tmp, sc)) {
+  if (!cta_select_sort_hi<kSelectPer>(list, hi, cnt, k_eff, sel, tmp, sc)) {
     const int got = cta_select_smallest_u64(list, cnt, k_eff, sel, sc);
     cta_sort_u64(sel, got, sc);
   }
