@@ -141,6 +141,29 @@ def test_fallback_table_in_chunks(hk, dev, dt, kind, mode):
     assert np.array_equal(s2.cpu().numpy().view(np.uint32), gs.view(np.uint32))
 
 
+def test_sampled_threshold_every_sample_count(hk, dev):
+    """Integer data at contexts that give every kind of sample count: M = ctx
+    (ctx <= 4096), M = 4096, M = ctx/128 between 4096 and 8192 (a ragged last
+    tile of samples) and M = 8192 (ctx >= 2^20). The thresholds decide the
+    candidate counts and the failed queries, which must equal the oracle's
+    filter simulation exactly; the selection is bit-exact."""
+    L = (1 << 20) + 5000
+    pos = np.array([L - 1, L - 2, (1 << 20) - 1, 1 << 20, 700001, 600000, 524287, 524288,
+                    524289, 300000, 5000, 4097, 3000, 900], np.int32)
+    case = si.random_case(L, len(pos), 16, 64, 512, "bf16", seed=71, positions=pos, kind="int")
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    rows = np.arange(len(pos))
+    compare(case, rows, gi, gs, exact=True)
+    stats = hk.read_stats(st)
+    fs = oracle.filter_sim(case, capacity=8 * 512)
+    assert stats["total_candidates"] == int(fs["cnt"].sum())
+    assert stats["n_failed"] == int(fs["failed"].sum())
+    assert stats["device_status"] == 0
+    counts = {oracle.sample_count(int(p) + 1) for p in pos}
+    assert {8192, 5468, 4687, 4096, 3001, 901} <= counts
+
+
 # ---- random workloads ---------------------------------------------------------------
 
 @pytest.mark.parametrize("L,n,H,d,k_top,dt,pos", [
