@@ -185,8 +185,9 @@ HYTOPK_API size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k
  * worked example); every causal key is scored on chip and keys with score >= T
  * are appended to the query's candidate buffer; queries with ctx > k and fewer
  * than k or more than `capacity` candidates are rescored over their whole
- * context; the candidates are radix-selected (score, then position) and
- * radix-sorted. */
+ * context (up to 64 of them one by one; past 64, every query, through
+ * score-table rows written into the workspace chunk by chunk); the candidates
+ * are radix-selected (score, then position) and radix-sorted. */
 HYTOPK_API hytopk_status hytopk_select(const void* q, const float* q_scale, const void* k,
                             const float* k_scale, const float* w, const int32_t* positions, int n,
                             int L, int H, int d, int k_top, hytopk_dtype dt, int32_t* idx_out,
