@@ -280,42 +280,48 @@ static __device__ void cta_sort_u64(uint64_t* sel, int n, RadixScratch& sc) {
   __syncthreads();
 }
 
-// Selection and order in one bucket pass, for lists of at most PER * blockDim.x
-// unique keys (a query's candidates in the common case). Only the upper 32
-// bits of each key (the score part) are held in registers: hi[r] is that of
-// list entry threadIdx.x + r * blockDim.x (loaded by the caller, who may read
-// past cnt: entries at or past cnt are ignored). The upper halves less their
-// minimum, shifted right until the range fits 4096 ordered buckets, give each
-// key a bucket; the buckets are counted and prefix-summed, which locates the
-// bucket b* holding the k_sel-th smallest key. The keys of buckets up to b*
-// are read again whole from the list and scattered by bucket into tmp; each
-// one's final place is its bucket's start plus the number of the bucket's
-// keys below it, and the places below k_sel are written to sel. The result is
-// the k_sel smallest keys in ascending order in sel[0 .. k_sel) -- the radix
-// select and sort of the list. Returns false, leaving sel untouched, when the
-// list is longer than PER * blockDim.x or a bucket holds more than kMaxBucket
-// keys (many equal scores); the caller then takes the general path. tmp needs
-// room for k_sel + kMaxBucket keys.
+// Selection and order in one bucket pass, for lists of at most PER * NT
+// unique keys (a query's candidates in the common case), NT = blockDim.x
+// threads. Only the upper 32 bits of each key (the score part) are held in
+// registers: hi[r] is that of list entry threadIdx.x + r * NT (loaded by the
+// caller, who may read past cnt: entries at or past cnt are ignored). The
+// upper halves less their minimum, shifted right until the range fits 4096
+// ordered buckets, give each key a bucket; the buckets are counted and
+// prefix-summed, which locates the bucket b* holding the k_sel-th smallest
+// key. The keys of buckets up to b* are read again whole from the list and
+// scattered by bucket into tmp; each one's final place is its bucket's start
+// plus the number of the bucket's keys below it, and the places below k_sel
+// are written to sel. The result is the k_sel smallest keys in ascending order
+// in sel[0 .. k_sel) -- the radix select and sort of the list. Returns false,
+// leaving sel untouched, when the list is longer than PER * NT or a bucket
+// holds more than kMaxBucket keys (many equal scores); the caller then takes
+// the general path. tmp needs room for k_sel + kMaxBucket keys.
+//
+// Thread t prefix-sums the buckets t * BPT .. t * BPT + BPT - 1 (BPT = 4096 /
+// NT). Bucket b is kept at hist[(b % BPT) * NT + b / BPT], so that the BPT
+// reads and writes of that sum are consecutive across each warp (no bank
+// conflicts); counts, cursors and bucket bounds go through the same map.
 constexpr uint32_t kMaxBucket = 32;
 
-template <int PER>
+template <int PER, int NT>
 static __device__ bool cta_select_sort_hi(const uint64_t* list, const uint32_t (&hi)[PER], int cnt,
                                           int k_sel, uint64_t* sel, uint64_t* tmp,
                                           RadixScratch& sc) {
-  constexpr int NB = 4096;
-  const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (cnt > PER * T) return false;
+  constexpr int NB = 4096, BPT = NB / NT;
+  static_assert(NB % NT == 0 && NT % 32 == 0 && NT / 32 <= 32, "thread count");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (cnt > PER * NT) return false;
   if (k_sel <= 0) return true;
   if (tid == 0) {
     sc.out[0] = 0xffffffffu;
     sc.out[1] = 0u;
     sc.out[2] = 0u;
   }
-  for (int b = tid; b < NB; b += T) sc.hist[b] = 0u;
+  for (int b = tid; b < NB; b += NT) sc.hist[b] = 0u;
   uint32_t lo = 0xffffffffu, top = 0u;
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    if (tid + r * T < cnt) {
+    if (tid + r * NT < cnt) {
       lo = min(lo, hi[r]);
       top = max(top, hi[r]);
     }
@@ -335,16 +341,17 @@ static __device__ bool cta_select_sort_hi(const uint64_t* list, const uint32_t (
   const int width = range == 0u ? 0 : 32 - __clz(range);
   const int sh = width > 12 ? width - 12 : 0;
   auto bucket = [&](uint32_t h) { return (h - kmin) >> sh; };
+  auto slot = [](uint32_t b) { return (b % BPT) * NT + b / BPT; };
 #pragma unroll
   for (int r = 0; r < PER; ++r)
-    if (tid + r * T < cnt) atomicAdd(&sc.hist[bucket(hi[r])], 1u);
+    if (tid + r * NT < cnt) atomicAdd(&sc.hist[slot(bucket(hi[r]))], 1u);
   __syncthreads();
   // exclusive prefix sum; the bucket where the running count reaches k_sel;
   // the largest bucket
-  const int per = (NB + T - 1) / T, b0 = tid * per, b1 = min(b0 + per, NB);
   uint32_t local = 0, big = 0;
-  for (int b = b0; b < b1; ++b) {
-    const uint32_t c = sc.hist[b];
+#pragma unroll 1
+  for (int j = 0; j < BPT; ++j) {
+    const uint32_t c = sc.hist[j * NT + tid];
     local += c;
     big = max(big, c);
   }
@@ -360,30 +367,31 @@ static __device__ bool cta_select_sort_hi(const uint64_t* list, const uint32_t (
   __syncthreads();
   uint32_t run = incl - local;
   for (int w = 0; w < warp; ++w) run += sc.warp_sums[w];
-  for (int b = b0; b < b1; ++b) {
-    const uint32_t c = sc.hist[b];
-    if (run < (uint32_t)k_sel && (uint32_t)k_sel <= run + c) sc.out[3] = (uint32_t)b;
-    sc.hist[b] = run;
+#pragma unroll 1
+  for (int j = 0; j < BPT; ++j) {
+    const uint32_t c = sc.hist[j * NT + tid];
+    if (run < (uint32_t)k_sel && (uint32_t)k_sel <= run + c) sc.out[3] = (uint32_t)(tid * BPT + j);
+    sc.hist[j * NT + tid] = run;
     run += c;
   }
   const bool crowded = sc.out[2] > kMaxBucket;
-  __syncthreads();  // hist[b] = start of bucket b; out[3] = b*
+  __syncthreads();  // hist = start of each bucket; out[3] = b*
   if (crowded) return false;
   const uint32_t bstar = sc.out[3];
 #pragma unroll
   for (int r = 0; r < PER; ++r) {
-    const int i = tid + r * T;
+    const int i = tid + r * NT;
     if (i < cnt) {
       const uint32_t b = bucket(hi[r]);
-      if (b <= bstar) tmp[atomicAdd(&sc.hist[b], 1u)] = __ldg(list + i);
+      if (b <= bstar) tmp[atomicAdd(&sc.hist[slot(b)], 1u)] = __ldg(list + i);
     }
   }
-  __syncthreads();  // hist[b] = end of bucket b (for b <= b*)
-  const uint32_t scattered = sc.hist[bstar];
-  for (uint32_t j = tid; j < scattered; j += T) {
+  __syncthreads();  // hist = end of each bucket up to b*
+  const uint32_t scattered = sc.hist[slot(bstar)];
+  for (uint32_t j = tid; j < scattered; j += NT) {
     const uint64_t key = tmp[j];
     const uint32_t b = bucket((uint32_t)(key >> 32));
-    const uint32_t start = b > 0 ? sc.hist[b - 1] : 0u, end = sc.hist[b];
+    const uint32_t start = b > 0 ? sc.hist[slot(b - 1)] : 0u, end = sc.hist[slot(b)];
     uint32_t dst = start;
     for (uint32_t m = start; m < end; ++m) dst += tmp[m] < key ? 1u : 0u;
     if (dst < (uint32_t)k_sel) sel[dst] = key;

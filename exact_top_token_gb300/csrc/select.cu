@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kSelectThreads, 3) k_select_candidates(Problem
   const int cnt = min(ws.cnt[slot], ws.C);
   if (t < 0 || n_failed > HYTOPK_MAX_RECOVERY_ROWS || failed) return;
   const int k_eff = min(p.k_top, cnt);
-  if (!cta_select_sort_hi<kSelectPer>(list, hi, cnt, k_eff, sel, tmp, sc)) {
+  if (!cta_select_sort_hi<kSelectPer, kSelectThreads>(list, hi, cnt, k_eff, sel, tmp, sc)) {
     const int got = cta_select_smallest_u64(list, cnt, k_eff, sel, sc);
     cta_sort_u64(sel, got, sc);
   }
