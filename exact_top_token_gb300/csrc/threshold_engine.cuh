@@ -16,9 +16,9 @@
 //                filter, then the sample's ordered key desc32(score) stored
 //                into tensor memory, one column per tile
 //   warps 4..7   select: the r-th smallest key of the query's M keys, read
-//                back from tensor memory (MSB-first radix select, 8-bit
-//                digits, shared-memory histogram), while the other roles
-//                already work on the next queries
+//                back from tensor memory (radix select over 2048 bins that
+//                span the keys' own range, shared-memory histogram), while
+//                the other roles already work on the next queries
 // Two key buffers of 64 TMEM columns (M <= 8192 = 64 x 128) sit beside the
 // two accumulators, so a query's keys are selected while the next query's are
 // written. Scores are those of the filter, bit for bit (stream::HeadSum,
@@ -40,6 +40,8 @@ constexpr int kSlots = 2;                          // TMEM accumulators
 constexpr int kKeyCols = kMaxSamples / kTileKeys;  // key columns per buffer
 constexpr int kSelBar = 2;                         // named barrier of the select warps
 constexpr int kSelThreads = 128;
+constexpr int kSelBins = 2048;                     // radix bins of the select
+constexpr int kSelBinsPer = kSelBins / kSelThreads;  // bins prefix-summed per thread
 
 struct TArgs {
   const void* k;
@@ -70,9 +72,9 @@ struct TCfg {
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = ((2 * QBYTES + 1023) / 1024) * 1024;
   static constexpr int W_OFF = RING_OFF + STAGES * KT_BYTES;  // [2][NQ] fp32
-  static constexpr int HIST_OFF = W_OFF + 2 * NQ * 4;         // [256] u32
-  static constexpr int SEL_OFF = HIST_OFF + 256 * 4;          // [8] u32
-  static constexpr int BAR_OFF = SEL_OFF + 32;
+  static constexpr int HIST_OFF = W_OFF + 2 * NQ * 4;         // [kSelBins] u32
+  static constexpr int SEL_OFF = HIST_OFF + kSelBins * 4;     // [16] u32
+  static constexpr int BAR_OFF = SEL_OFF + 64;
   // full/empty stages, accumulators, q buffers, key buffers
   static constexpr int NBARS = 2 * STAGES + 2 * kSlots + 4 + 4;
   static constexpr int MISC_OFF = BAR_OFF + 8 * NBARS;        // TMEM base, abort flag
@@ -104,79 +106,104 @@ __device__ __forceinline__ TQ thr_query(const TArgs& a, int slot) {
   return q;
 }
 
-// The kk-th smallest (1-based) of the keys in columns [0, ncols) of the key
-// buffer at kcol (this thread's TMEM lane: the select warps cover the 128
-// lanes). MSB-first radix select with 8-bit digits; once the bin holding the
-// kk-th key holds it alone, that key is read under its prefix. All 128 select
-// threads call it.
-__device__ __forceinline__ uint32_t tmem_kth_smallest(uint32_t kcol, int ncols, uint32_t kk,
+// The kk-th smallest (1-based) of a query's M sample keys in the key buffer
+// at kcol: sample j sits in column j / 128, TMEM lane j % 128 (the select
+// warps cover the 128 lanes; thread st reads lane st). Radix select whose
+// digit follows the keys' range: a first sweep finds their minimum and
+// maximum, then each pass splits the current range [base, base + 2^width)
+// into kSelBins bins of equal width, counts the keys in each (bin b kept at
+// hist[(b % kSelBinsPer) * 128 + b / kSelBinsPer], so that each thread's
+// prefix sum over its kSelBinsPer bins reads them without bank conflicts) and
+// narrows the range to the bin holding the kk-th key -- until that bin is one
+// key wide or holds the kk-th key alone. Scores spread over a few exponents
+// fill the bins of the first pass evenly, so one pass and a sweep to fetch
+// the lone key usually suffice. sh: 16 words of shared scratch. All 128
+// select threads call it.
+__device__ __forceinline__ uint32_t tmem_kth_smallest(uint32_t kcol, int M, uint32_t kk,
                                                       uint32_t* hist, uint32_t* sh) {
   const int st = (int)threadIdx.x - kSelWarp0 * 32, lane = st & 31, sw = st >> 5;
-  uint32_t prefix = 0;
-  int done = 0;
-  for (int p = 0; p < 4; ++p) {
-    const int shift = 24 - 8 * p;
-    for (int b = st; b < 256; b += kSelThreads) hist[b] = 0;
-    tc::bar_sync(kSelBar, kSelThreads);
+  const int ncols = (M + kTileKeys - 1) / kTileKeys;
+  // f(key) for each of this lane's sample keys (padding rows past M skipped)
+  auto sweep = [&](auto&& f) {
     for (int c0 = 0; c0 < ncols; c0 += 16) {
       uint32_t v[16];
       tc::tmem_ld16u(kcol + (uint32_t)c0, v);
       tc::tmem_wait_ld(v);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const bool in = c0 + u < ncols && (done == 0 || (v[u] >> (32 - done)) == prefix);
-        hist_add(hist, (v[u] >> shift) & 255u, in);
+      for (int u = 0; u < 16; ++u)
+        if ((c0 + u) * kTileKeys + st < M) f(v[u]);
+    }
+  };
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  sweep([&](uint32_t v) {
+    lo = min(lo, v);
+    hi = max(hi, v);
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  if (lane == 0) {
+    sh[sw] = lo;
+    sh[4 + sw] = hi;
+  }
+  tc::bar_sync(kSelBar, kSelThreads);
+  uint32_t base = min(min(sh[0], sh[1]), min(sh[2], sh[3]));
+  const uint32_t top = max(max(sh[4], sh[5]), max(sh[6], sh[7]));
+  int width = top == base ? 0 : 32 - __clz(top - base);  // keys in [base, base + 2^width)
+  while (width > 0) {
+    const int sft = width > 11 ? width - 11 : 0;
+    for (int b = st; b < kSelBins; b += kSelThreads) hist[b] = 0u;
+    tc::bar_sync(kSelBar, kSelThreads);
+    sweep([&](uint32_t v) {
+      const uint32_t off = v - base;
+      if (v >= base && (width >= 32 || (off >> width) == 0u)) {
+        const uint32_t bin = off >> sft;
+        atomicAdd(hist + (bin % kSelBinsPer) * kSelThreads + bin / kSelBinsPer, 1u);
       }
+    });
+    tc::bar_sync(kSelBar, kSelThreads);
+    uint32_t local = 0;
+#pragma unroll
+    for (int j = 0; j < kSelBinsPer; ++j) local += hist[j * kSelThreads + st];
+    uint32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
+    }
+    if (lane == 31) sh[8 + sw] = incl;
+    tc::bar_sync(kSelBar, kSelThreads);
+    uint32_t run = incl - local;
+    for (int w = 0; w < sw; ++w) run += sh[8 + w];
+#pragma unroll
+    for (int j = 0; j < kSelBinsPer; ++j) {
+      const uint32_t c = hist[j * kSelThreads + st];
+      if (run < kk && kk <= run + c) {
+        sh[12] = (uint32_t)(st * kSelBinsPer + j);
+        sh[13] = run;
+        sh[14] = c;
+      }
+      run += c;
     }
     tc::bar_sync(kSelBar, kSelThreads);
-    if (sw == 0) {  // the bin where the running count reaches kk (8 bins a lane)
-      uint32_t loc[8], tot = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        loc[i] = hist[lane * 8 + i];
-        tot += loc[i];
-      }
-      uint32_t incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += x;
-      }
-      uint32_t cum = incl - tot;
-      if (cum < kk && kk <= incl) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (cum < kk && kk <= cum + loc[i]) {
-            sh[4] = (uint32_t)(lane * 8 + i);
-            sh[5] = cum;
-          }
-          cum += loc[i];
-        }
-      }
-    }
-    tc::bar_sync(kSelBar, kSelThreads);
-    const uint32_t bin = sh[4], before = sh[5];
-    const bool alone = hist[bin] == 1u;
+    const uint32_t bstar = sh[12], before = sh[13], cnt = sh[14];
     kk -= before;
-    prefix = (prefix << 8) | bin;
-    done += 8;
-    tc::bar_sync(kSelBar, kSelThreads);  // sh and hist read before they are reused
-    if (alone && done < 32) {
-      for (int c0 = 0; c0 < ncols; c0 += 16) {
-        uint32_t v[16];
-        tc::tmem_ld16u(kcol + (uint32_t)c0, v);
-        tc::tmem_wait_ld(v);
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          if (c0 + u < ncols && (v[u] >> (32 - done)) == prefix) sh[6] = v[u];
-      }
+    base += bstar << sft;
+    width = sft;
+    if (width > 0 && cnt == 1u) {  // the kk-th key is alone in its bin: fetch it
+      sweep([&](uint32_t v) {
+        if (v >= base && ((v - base) >> width) == 0u) sh[15] = v;
+      });
       tc::bar_sync(kSelBar, kSelThreads);
-      const uint32_t key = sh[6];
-      tc::bar_sync(kSelBar, kSelThreads);
-      return key;
+      base = sh[15];
+      width = 0;
     }
   }
-  return prefix;
+  // every thread is past its reads of sh and hist before they are reused
+  tc::bar_sync(kSelBar, kSelThreads);
+  return base;
 }
 
 template <int D, int DT, int H>
@@ -324,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_threshold(const TArgs a) {
       tc::fence_after_sync();
       const uint32_t kcol =
           tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(C_::ACC_COLS + b * kKeyCols);
-      const uint32_t v = tmem_kth_smallest(kcol, q.ntiles, (uint32_t)q.r, hist, sel_sh);
+      const uint32_t v = tmem_kth_smallest(kcol, q.M, (uint32_t)q.r, hist, sel_sh);
       if (st == 0) a.thr[slot] = desc32_score(v);
       tc::fence_before_sync();
       __syncwarp();
