@@ -197,6 +197,33 @@ struct SampleStep {
   }
 };
 
+// The positions of samples j0, j0 + 128, j0 + 256, ... of one query, one per
+// next() (the caller tells the samples past M apart), with no division per
+// sample: with 128 b = dq M + dr, p(j + 128) = p(j) + 128 a + dq, plus one
+// when the remainder of j b / M passes M.
+struct SampleWalk {
+  uint32_t p, rem, dp, dr, m;
+  __device__ __forceinline__ void init(const SampleStep& st, int j0) {
+    m = st.m;
+    const uint32_t jb = (uint32_t)j0 * st.b, q0 = jb / m;
+    p = (uint32_t)j0 * st.a + q0;
+    rem = jb - q0 * m;
+    const uint32_t tb = (uint32_t)kTileKeys * st.b, dq = tb / m;
+    dp = (uint32_t)kTileKeys * st.a + dq;
+    dr = tb - dq * m;
+  }
+  __device__ __forceinline__ int next() {
+    const int s = (int)p;
+    p += dp;
+    rem += dr;
+    if (rem >= m) {
+      rem -= m;
+      ++p;
+    }
+    return s;
+  }
+};
+
 // Entries of the shared-memory sort buffer for k keys: the next power of two,
 // at least 2 (so that what follows it stays 16-byte aligned).
 __host__ __device__ __forceinline__ int sort_capacity(int k) {

@@ -288,7 +288,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_threshold(const TArgs a) {
         wq_s[b * NQ + h] = h < H ? __ldg(a.wq + (size_t)slot * H + h) : 0.0f;
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(q_full + b);
-      auto key_of = [&](int j) -> int { return j < q.M ? q.step.at(j) : -1; };
+      SampleWalk walk;  // this lane's sample of each tile
+      walk.init(q.step, tid);
+      auto key_of = [&](int j) -> int {  // sample j = next tile's, -1 past M
+        const int s = walk.next();
+        return j < q.M ? s : -1;
+      };
       int npend = 0;
       int s_next = key_of(tid), s_next2 = key_of(kTileKeys + tid);
       bool ok = true;
@@ -379,7 +384,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_threshold(const TArgs a) {
       tc::fence_after_sync();
       const float* wq = wq_s + b * NQ;
       const uint32_t kcol = tmem_base + lane_off + (uint32_t)(C_::ACC_COLS + b * kKeyCols);
-      auto key_of = [&](int j) -> int { return j < q.M ? q.step.at(j) : -1; };
+      SampleWalk walk;  // this thread's sample of each tile
+      walk.init(q.step, row);
+      auto key_of = [&](int j) -> int {  // sample j = next tile's, -1 past M
+        const int s = walk.next();
+        return j < q.M ? s : -1;
+      };
       int s_next = key_of(row), s_next2 = key_of(kTileKeys + row);
       float ks_next = scale_of(s_next);
       bool ok = true;
