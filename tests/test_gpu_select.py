@@ -181,6 +181,8 @@ def test_sampled_threshold_every_sample_count(hk, dev):
     (3000, 30, 16, 64, 200, "e4m3_bf16", "last"),
     (9000, 20, 1, 64, 100, "bf16", "random"),      # one head
     (12000, 24, 4, 128, 300, "e4m3", "random"),    # four heads, 128-byte rows
+    (20000, 20, 128, 128, 256, "e4m3", "random"),  # 128 heads, 4096 samples
+    (15000, 16, 128, 128, 512, "bf16", "random"),  # 128 heads, 256-byte rows
 ])
 def test_random_small(hk, dev, L, n, H, d, k_top, dt, pos):
     case = si.random_case(L, n, H, d, k_top, dt, seed=L + n, positions=pos)
