@@ -154,7 +154,11 @@ cudaError_t launch_prep(const Problem& p, const SelectWs& ws, cudaStream_t st) {
     k_rank_by_position<<<(p.n + per_block - 1) / per_block, kRankWarps * 32, 0, st>>>(
         p.positions, p.n, p.L, ws.perm);
   if (ws.n_pad > 0) k_pack_queries<<<ws.n_pad, 128, 0, st>>>(p, ws);
-  if (p.dt == 1) k_check_key_scales<<<64, 256, 0, st>>>(p.k_scale, p.L, ws.counters);
+  if (p.dt == 1) {
+    // four blocks per SM (about 16 scales a thread at 1M keys), fewer when L is small
+    const int want = (p.L + 4 * 256 - 1) / (4 * 256), cap = 4 * num_sms();
+    k_check_key_scales<<<want < cap ? want : cap, 256, 0, st>>>(p.k_scale, p.L, ws.counters);
+  }
   return cudaGetLastError();
 }
 

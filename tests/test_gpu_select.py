@@ -321,6 +321,27 @@ def test_all_equal_scores_and_edge_rows(hk, dev):
 
 # ---- replay ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("which,bad", [("k", 0.0), ("k", -1.0), ("q", 0.0), ("q", -1.0)])
+def test_bad_scale_sets_status(hk, dev, which, bad):
+    """A key or query scale that is not > 0 sets the bad-scale status bit; with
+    valid scales the bit stays clear. The key scales of 1M keys are checked by
+    a grid of many blocks, so the bad one sits near the end."""
+    L = 300000 if which == "k" else 4000
+    case = si.random_case(L, 8, 8, 64, 64, "e4m3", seed=7, positions="random")
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    assert hk.read_stats(st)["device_status"] == 0
+    if which == "k":
+        ks = case["k_scale"].copy()
+        ks[L - 3] = bad
+        bad_case = dict(case, k_scale=ks)
+    else:
+        qs = case["q_scale"].copy()
+        qs[5, 3] = bad
+        bad_case = dict(case, q_scale=qs)
+    idx, sc, st, _ = run_select(hk, bad_case, dev, stats=True)
+    assert hk.read_stats(st)["device_status"] & hk.DEV_BAD_SCALE
+
+
 def test_replay_parity_and_bad_indices(hk, dev):
     import torch
 
