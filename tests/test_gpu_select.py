@@ -201,6 +201,24 @@ def test_mixed_contexts_full(hk, dev):
     assert int((case["positions"] + 1 <= case["k_top"]).sum()) > 0  # some select-all rows
 
 
+
+@pytest.mark.slow
+def test_large_batch_64bit_offsets(hk, dev):
+    """131072 queries with room for 32768 candidates each: slot x capacity
+    passes 2^31 (and the candidate buffer's byte offsets 2^32) for half of the
+    slots. 32 sampled rows against the oracle, structure on 4096 sampled rows,
+    no device status."""
+    n, L, H, d, k_top, cap = 131072, 32768, 8, 64, 256, 32768
+    case = si.random_case(L, n, H, d, k_top, "bf16", seed=13, positions="random")
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True, capacity=cap)
+    gi, gs = host(idx, sc)
+    stats = hk.read_stats(st)
+    assert stats["device_status"] == 0 and stats["n_queries"] == n
+    rows = si.sampled_rows(n, 32)
+    compare(case, rows, gi[rows], gs[rows])
+    many = si.sampled_rows(n, 4096)
+    check_structure(gi[many], gs[many], case["positions"][many], k_top)
+
 @pytest.fixture(scope="module")
 def glm_run(hk, dev):
     """The 1M-key workload selected once and its indices replayed once."""
