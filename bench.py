@@ -355,6 +355,10 @@ def fallback_chunks(n, L, k_top, capacity=0):
     n_pad = (n + 511) // 512 * 512
     C = capacity or 8 * k_top
     rows = (al(n_pad * C * 8) + al(64 * L * 4)) // (L * 4)
+    if rows > 304:  # whole waves of the read-back's 304 CTAs, if no more chunks
+        waves = rows - rows % 304
+        if -(-n // waves) == -(-n // rows):
+            rows = waves
     rows = min(rows, n)
     return (n + rows - 1) // rows if n else 0
 

@@ -192,7 +192,14 @@ hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* 
     // chunk by chunk. Whether that happens is known only on the device, so
     // these launches are always made and return at once without a fallback.
     float* table = reinterpret_cast<float*>(base + lay.cand);
-    const size_t rows_fit = (lay.plan - lay.cand) / ((size_t)L * 4);
+    // Chunks of whole read-back waves (kTableCtas rows, one per CTA) when
+    // that takes no more chunks: a chunk a few rows past a wave leaves those
+    // rows to a second pass of the CTAs that took them.
+    size_t rows_fit = (lay.plan - lay.cand) / ((size_t)L * 4);
+    if (rows_fit > (size_t)kTableCtas) {
+      const size_t waves = rows_fit - rows_fit % kTableCtas;
+      if ((n + waves - 1) / waves == (n + rows_fit - 1) / rows_fit) rows_fit = waves;
+    }
     const int chunk = (int)(rows_fit < (size_t)n ? rows_fit : (size_t)n);
     FallbackMaps maps;
     HYTOPK_TRY(prepare_fallback_table(p, ws, &maps));
