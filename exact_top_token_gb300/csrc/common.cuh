@@ -16,7 +16,6 @@
 
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "hytopk.h"
@@ -70,51 +69,6 @@ struct SelectWs {
   int32_t* plan;        // [nchunks + 1] filter work items per key chunk
   int n_pad, C;
 };
-
-// ---- element decoding --------------------------------------------------------
-
-__device__ __forceinline__ float bf16_value(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
-
-__device__ __forceinline__ float e4m3_value(uint8_t c) {
-  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
-  return __half2float(__half(h));
-}
-
-// Load key row s (D elements) as floats, raw (no scale).
-template <int D, int DT>
-__device__ __forceinline__ void load_key_row(const void* kbase, size_t s, float (&kr)[D]) {
-  if (DT == 0) {
-    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(kbase) + s * D);
-#pragma unroll
-    for (int v = 0; v < D / 8; ++v) {
-      uint4 x = __ldg(src + v);
-      uint32_t wv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        kr[v * 8 + 2 * j] = __uint_as_float(wv[j] << 16);
-        kr[v * 8 + 2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
-      }
-    }
-  } else {
-    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(kbase) + s * D);
-#pragma unroll
-    for (int v = 0; v < D / 16; ++v) {
-      uint4 x = __ldg(src + v);
-      uint32_t wv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) kr[v * 16 + 4 * j + b] = e4m3_value((wv[j] >> (8 * b)) & 0xFF);
-    }
-  }
-}
-
-// Decode one (query, head) row of D raw elements into shared memory.
-template <int DT>
-__device__ __forceinline__ float load_elem(const void* base, size_t i) {
-  if (DT == 0) return bf16_value(reinterpret_cast<const uint16_t*>(base)[i]);
-  return e4m3_value(reinterpret_cast<const uint8_t*>(base)[i]);
-}
 
 // ---- the score ------------------------------------------------------------------
 

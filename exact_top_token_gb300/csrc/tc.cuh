@@ -365,17 +365,5 @@ struct Geo {
   }
 };
 
-// ---- packed fp32 FMA (two lanes per instruction) ----------------------------------------
-
-__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float w0,
-                                     float w1) {
-  uint64_t acc, x, w;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(w) : "f"(w0), "f"(w1));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(x), "l"(w));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
-}
-
 }  // namespace tc
 }  // namespace hytopk
