@@ -56,7 +56,7 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, int dt, uint64_t inner_ele
                   uint32_t box_inner_elems, uint32_t box_rows, int swizzle_bytes);
 int num_sms();
 int stream_chunks(int L);
-cudaError_t launch_plan(const SelectWs& ws, int L, int qb, cudaStream_t st);
+cudaError_t launch_plan(const SelectWs& ws, int L, int qb, int chunk_tiles, cudaStream_t st);
 
 // Shared-memory bytes of the candidate selection for k_top.
 size_t select_smem_bytes(int k_top);

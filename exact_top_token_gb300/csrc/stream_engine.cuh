@@ -7,7 +7,10 @@
 // small per-query candidate buffer (atomic appends). Score-table paragraph:
 // the conventional method writes every score to HBM instead (MODE 1 here).
 //
-// Work item = (key chunk of 64 tiles x 128 keys, query block of QB slots).
+// Work item = (key chunk of 64 or 256 tiles x 128 keys, query block of QB
+// slots); the filter takes the longer chunks when there are work items enough
+// for every SM without them (long contexts), since each item boundary costs a
+// reload of the block's query operand and weights.
 // One persistent CTA per SM walks items blockIdx.x, +gridDim.x, ... in
 // chunk-major order, so the CTAs running at one time share a key chunk in L2.
 //
@@ -30,7 +33,8 @@
 namespace hytopk {
 namespace stream {
 
-constexpr int kChunkTiles = 64;
+constexpr int kChunkTiles = 64;       // tiles per key chunk (the score table, short contexts)
+constexpr int kChunkTilesLong = 256;  // the filter at long contexts
 constexpr int kChunkKeys = kChunkTiles * kTileKeys;
 constexpr int kEpiWarps = 16;   // epilogue warps (4 per TMEM lane quadrant)
 constexpr int kEpiWarp0 = 4;    // first epilogue warp: warpgroups 1..4 are the epilogue
@@ -47,6 +51,14 @@ constexpr int kRegsEpi = 112;
 static_assert(128 * kRegsCtl + (kThreads - 128) * kRegsEpi <= kThreads * kRegsLaunch,
               "register split exceeds the CTA's launch allocation");
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA (and its 512 TMEM columns) per SM
+
+// Candidate staging entries per query slot and work item of the filter: 1024
+// per block of QB slots, and for 16 <= H <= 32 (whose warps stage into private
+// regions of a quarter of this, flushed when full) at least 32 a region.
+__host__ __device__ constexpr int stage_capacity(int H, int QB) {
+  return (1024 / QB) > ((H >= 16 && H <= 32) ? 128 : 8) ? (1024 / QB)
+                                                          : ((H >= 16 && H <= 32) ? 128 : 8);
+}
 
 template <int D, int DT, int H, int MODE_STAGING = 1>
 struct Cfg {
@@ -71,10 +83,7 @@ struct Cfg {
   static constexpr int THR_OFF = POS_OFF + QB * 4;
   static constexpr int ROW_OFF = THR_OFF + QB * 4;
   // per-item candidate staging (filter): CAP entries per query slot of the block
-  // (for 16 <= H <= 32, whose warps stage into private regions of
-  // STAGE_CAP / 4 entries flushed when full, at least 32 entries a region)
-  static constexpr int STAGE_CAP_MIN = (H >= 16 && H <= 32) ? 128 : 8;
-  static constexpr int STAGE_CAP = (1024 / QB) > STAGE_CAP_MIN ? (1024 / QB) : STAGE_CAP_MIN;
+  static constexpr int STAGE_CAP = stage_capacity(H, QB);
   static constexpr int SCNT_OFF = ROW_OFF + QB * 4;
   static constexpr int STAGE_OFF = ((SCNT_OFF + QB * 4) + 15) / 16 * 16;
   static constexpr int END = STAGE_OFF + (MODE_STAGING ? QB * STAGE_CAP * 8 : 0);
@@ -99,6 +108,7 @@ struct Args {
   int32_t* cnt;
   uint64_t* cand;
   const int32_t* plan;  // [nchunks + 1] item offsets per key chunk
+  int chunk_tiles;      // tiles per key chunk (kChunkTiles or kChunkTilesLong)
   int C;
   int n_pad;
   int reverse;
@@ -139,18 +149,19 @@ template <int QB, int MODE>
 __device__ __forceinline__ Item decode(const Args& a, int nchunks, int nblocks, int it) {
   Item r;
   int c;
+  const int ct = a.chunk_tiles;
   if (MODE == 0) {
     c = find_chunk(a.plan, nchunks, it);
     r.block = it - __ldg(a.plan + c);
     const int maxpos = __ldg(a.qpos + r.block * QB);
-    r.tile0 = c * kChunkTiles;
+    r.tile0 = c * ct;
     const int end = min(maxpos + 1, a.L);
-    r.ntiles = min(kChunkTiles, (end - r.tile0 * kTileKeys + kTileKeys - 1) / kTileKeys);
+    r.ntiles = min(ct, (end - r.tile0 * kTileKeys + kTileKeys - 1) / kTileKeys);
   } else {
     c = it / nblocks;
     r.block = it - c * nblocks;
-    r.tile0 = c * kChunkTiles;
-    r.ntiles = min(kChunkTiles, (a.L - r.tile0 * kTileKeys + kTileKeys - 1) / kTileKeys);
+    r.tile0 = c * ct;
+    r.ntiles = min(ct, (a.L - r.tile0 * kTileKeys + kTileKeys - 1) / kTileKeys);
   }
   return r;
 }
@@ -394,7 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<const volatile uint32_t*>(a.gate) <= HYTOPK_MAX_RECOVERY_ROWS)
     return;  // uniform over the grid, before any barrier or TMEM is set up
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nchunks = (a.L + kChunkKeys - 1) / kChunkKeys;
+  const int chunk_keys = a.chunk_tiles * kTileKeys;
+  const int nchunks = (a.L + chunk_keys - 1) / chunk_keys;
   const int nblocks = MODE == 0 ? a.n_pad / QB : (a.rows + QB - 1) / QB;
   const int total = MODE == 0 ? __ldg(a.plan + nchunks) : nchunks * nblocks;
 

@@ -56,9 +56,21 @@ cudaError_t launch_filter(const Problem& p, const SelectWs& ws, int reverse, cud
                     atom_bytes(p) / es, 256, atom_bytes(p)))
     return cudaErrorInvalidValue;
   const int qb = stream_query_block(p.H, p.d, p.dt);
-  cudaError_t e = launch_plan(ws, p.L, qb, st);
+  // The long key chunks (fewer item boundaries, each a reload of the block's
+  // query operand and weights) when they still leave 64 work items per SM
+  // before the causal cut, and when a query's expected candidates per item
+  // (about 3k of its keys pass, spread over a context of up to L keys) fit
+  // its staging room (past it, keys take one global atomic each).
+  const int long_keys = stream::kChunkTilesLong * kTileKeys;
+  const int64_t long_items = (int64_t)(ws.n_pad / qb) * ((p.L + long_keys - 1) / long_keys);
+  const double per_item = 3.0 * p.k_top * (double)long_keys / (double)p.L;
+  const bool long_chunks = long_items >= 64LL * num_sms() &&
+                           per_item <= (double)stream::stage_capacity(p.H, qb);
+  const int chunk_tiles = long_chunks ? stream::kChunkTilesLong : stream::kChunkTiles;
+  cudaError_t e = launch_plan(ws, p.L, qb, chunk_tiles, st);
   if (e != cudaSuccess) return e;
   stream::Args a{};
+  a.chunk_tiles = chunk_tiles;
   a.qpos = ws.qpos;
   a.thr = ws.thr;
   a.wq = ws.wq;
@@ -90,6 +102,7 @@ cudaError_t launch_fallback_table(const Problem& p, const SelectWs& ws, const Fa
   const CUtensorMap& km = m.km;
   const CUtensorMap& qm = m.qm;
   stream::Args a{};
+  a.chunk_tiles = stream::kChunkTiles;
   a.wq = ws.wq;  // halved folded weights in slot order
   a.positions = ws.qpos;
   a.table = table;
@@ -113,6 +126,7 @@ cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, con
                     atom_bytes(p)))
     return cudaErrorInvalidValue;
   stream::Args a{};
+  a.chunk_tiles = stream::kChunkTiles;
   a.wq = hw;
   a.w = p.w;
   a.q_scale = p.q_scale;

@@ -46,14 +46,15 @@ __device__ int block_exclusive_scan(int v, int* excl, int* warp_tot) {
 // item per query block whose largest position reaches the chunk (blocks are
 // sorted by position, descending, so they are a prefix). plan[nchunks] = total.
 __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ qpos, int nblocks,
-                                               int qb, int nchunks, int32_t* __restrict__ plan) {
+                                               int qb, int nchunks, int chunk_keys,
+                                               int32_t* __restrict__ plan) {
   __shared__ int warp_tot[32];
   int carry = 0;
   for (int base = 0; base < nchunks; base += 1024) {
     const int c = base + threadIdx.x;
     int nb = 0;
     if (c < nchunks) {
-      const int key0 = c * stream::kChunkKeys;
+      const int key0 = c * chunk_keys;
       int lo = 0, hi = nblocks;
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
@@ -97,10 +98,14 @@ int num_sms() {
   return n;
 }
 
+// Key chunks at the shortest chunk length: an upper bound on the filter's
+// chunk count (the size of the plan).
 int stream_chunks(int L) { return (L + stream::kChunkKeys - 1) / stream::kChunkKeys; }
 
-cudaError_t launch_plan(const SelectWs& ws, int L, int qb, cudaStream_t st) {
-  k_plan<<<1, 1024, 0, st>>>(ws.qpos, ws.n_pad / qb, qb, stream_chunks(L), ws.plan);
+cudaError_t launch_plan(const SelectWs& ws, int L, int qb, int chunk_tiles, cudaStream_t st) {
+  const int chunk_keys = chunk_tiles * kTileKeys;
+  k_plan<<<1, 1024, 0, st>>>(ws.qpos, ws.n_pad / qb, qb, (L + chunk_keys - 1) / chunk_keys,
+                             chunk_keys, ws.plan);
   return cudaGetLastError();
 }
 
