@@ -219,6 +219,23 @@ def test_large_batch_64bit_offsets(hk, dev):
     many = si.sampled_rows(n, 4096)
     check_structure(gi[many], gs[many], case["positions"][many], k_top)
 
+
+@pytest.mark.slow
+def test_long_work_items_ragged_context(hk, dev):
+    """2048 queries at random positions over 700,001 keys with H = 64: enough
+    work items for the filter's long (256-tile) key chunks, a last chunk cut
+    short by L and blocks cut short by their positions. 64 sampled rows
+    against the oracle, structure on every row, exact statistics shape."""
+    n, L, H, d, k_top = 2048, 700001, 64, 128, 1024
+    case = si.random_case(L, n, H, d, k_top, "e4m3", seed=21, positions="random")
+    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    gi, gs = host(idx, sc)
+    stats = hk.read_stats(st)
+    assert stats["device_status"] == 0 and stats["n_queries"] == n
+    rows = si.sampled_rows(n, 64)
+    compare(case, rows, gi[rows], gs[rows])
+    check_structure(gi, gs, case["positions"], k_top)
+
 @pytest.fixture(scope="module")
 def glm_run(hk, dev):
     """The 1M-key workload selected once and its indices replayed once."""
