@@ -191,7 +191,10 @@ def peaks():
 # ---- clocks during the timed region ---------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+    """nvidia-smi every 50 ms, started before the warm-up steps; stop(window)
+    keeps the samples whose timestamps fall in the timed region's wall-clock
+    window (host time.time() bounds), when there are any."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
               "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -205,11 +208,22 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp):
+        import datetime
+
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -221,15 +235,18 @@ class ClockSampler:
         rows = []
         for line in open(self.file.name):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 10:
+            if len(parts) < 11:
                 continue
             try:
-                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
-                             "util": float(parts[4]), "hw": parts[6], "hwt": parts[7],
-                             "swt": parts[8], "pcap": parts[9]})
+                rows.append({"t": self._when(parts[0]), "sm": float(parts[2]),
+                             "max": float(parts[3]), "util": float(parts[5]), "hw": parts[7],
+                             "hwt": parts[8], "swt": parts[9], "pcap": parts[10]})
             except ValueError:
                 continue
         os.unlink(self.file.name)
+        if window is not None:
+            inside = [r for r in rows if r["t"] is not None and window[0] <= r["t"] <= window[1]]
+            rows = inside or rows
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         busy = [r for r in rows if r["util"] >= 50] or rows
@@ -401,7 +418,7 @@ def gpu_arm(args, world, rank, local):
     if rank == 0:
         clocks.start()
     tm = time_steps(hk, case, t, ws, dev, args.steps, args.warmup, args.replay_group, world)
-    clk = clocks.stop() if rank == 0 else None
+    clk = clocks.stop(tm["wall"]) if rank == 0 else None
     idx, sc = tm["idx"], tm["scores"]
     ms_step = tm["ms_step"]
     phase_ms, replay_ms, select_ms = tm["phases_ms"], tm["replay_ms"], tm["select_ms"]
@@ -503,6 +520,7 @@ def time_steps(hk, case, t, ws, dev, steps, warmup, replay_group=1, world=1, sta
     flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
     start.record(stream)
     for i in range(steps):
         if flush:
@@ -510,11 +528,12 @@ def time_steps(hk, case, t, ws, dev, steps, warmup, replay_group=1, world=1, sta
         step(step_events[i])
     stop.record(stream)
     torch.cuda.synchronize()
+    wall1 = time.time()
     barrier(world)
     mine = (sum(ev[0].elapsed_time(ev[nph]) for ev in step_events) if flush
             else start.elapsed_time(stop))
     ms_total = max_over_ranks(mine, world, dev)
-    out = {"ms_step": ms_total / steps, "flushed": flush,
+    out = {"ms_step": ms_total / steps, "flushed": flush, "wall": (wall0, wall1),
            "phases_ms": {name: statistics.mean(ev[j].elapsed_time(ev[j + 1])
                                                for ev in step_events)
                          for j, name in enumerate(hk.PHASES)},
