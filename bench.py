@@ -67,7 +67,7 @@ WORKLOADS = {"glm_1m": si.glm_1m, "glm_1m_adjacent": si.glm_1m_adjacent,
 # files (profiles/glm_1m_last1024_filter_k_stream_ncu.txt gives the command).
 # Reported as roofline.traffic only while the running library is that build;
 # otherwise the traffic is reported as null.
-FILTER_TRAFFIC = {"glm_1m": {"bytes": 1157346304 + 397261056, "build": "3cbcdf8d4078"}}
+FILTER_TRAFFIC = {"glm_1m": {"bytes": 1196557312 + 397560832, "build": "a16bbb981209"}}
 FILTER_SOURCES = ("stream_engine.cuh", "stream_launch.cu", "stream_d128_e4m3.cu", "tc.cuh",
                   "common.cuh")
 

@@ -126,7 +126,13 @@ cudaError_t launch_table(const Problem& p, int row0, int rows, float* table, con
                     atom_bytes(p)))
     return cudaErrorInvalidValue;
   stream::Args a{};
-  a.chunk_tiles = stream::kChunkTiles;
+  // long key chunks when they still leave 64 work items per SM, as in the
+  // filter (every score is written, so no staging bound)
+  const int qb = stream_query_block(p.H, p.d, p.dt);
+  const int long_keys = stream::kChunkTilesLong * kTileKeys;
+  const int64_t long_items =
+      (int64_t)((rows + qb - 1) / qb) * ((p.L + long_keys - 1) / long_keys);
+  a.chunk_tiles = long_items >= 64LL * num_sms() ? stream::kChunkTilesLong : stream::kChunkTiles;
   a.wq = hw;
   a.w = p.w;
   a.q_scale = p.q_scale;
