@@ -223,18 +223,24 @@ def test_large_batch_64bit_offsets(hk, dev):
 @pytest.mark.slow
 def test_long_work_items_ragged_context(hk, dev):
     """2048 queries at random positions over 700,001 keys with H = 64: enough
-    work items for the filter's long (256-tile) key chunks, a last chunk cut
-    short by L and blocks cut short by their positions. 64 sampled rows
-    against the oracle, structure on every row, exact statistics shape."""
+    work items for the long (256-tile) key chunks of the filter and of the
+    two-pass table writer, a last chunk cut short by L and blocks cut short
+    by their positions. 64 sampled rows against the oracle, structure on
+    every row, and the two-pass path bit for bit the selection."""
     n, L, H, d, k_top = 2048, 700001, 64, 128, 1024
     case = si.random_case(L, n, H, d, k_top, "e4m3", seed=21, positions="random")
-    idx, sc, st, _ = run_select(hk, case, dev, stats=True)
+    idx, sc, st, t = run_select(hk, case, dev, stats=True)
     gi, gs = host(idx, sc)
     stats = hk.read_stats(st)
     assert stats["device_status"] == 0 and stats["n_queries"] == n
     rows = si.sampled_rows(n, 64)
     compare(case, rows, gi[rows], gs[rows])
     check_structure(gi, gs, case["positions"], k_top)
+    # the two-pass path's table writer takes the long chunks here too
+    i2, s2 = hk.select_twopass(t["q"], t["k"], t["w"], t["positions"], k_top,
+                               q_scale=t["q_scale"], k_scale=t["k_scale"])
+    assert np.array_equal(i2.cpu().numpy(), gi)
+    assert np.array_equal(s2.cpu().numpy().view(np.uint32), gs.view(np.uint32))
 
 @pytest.fixture(scope="module")
 def glm_run(hk, dev):
