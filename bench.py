@@ -64,7 +64,7 @@ WORKLOADS = {"glm_1m": si.glm_1m, "glm_1m_adjacent": si.glm_1m_adjacent,
 # DRAM bytes (read + write) of one full-size filter launch, from one ncu
 # capture of the filter kernel (dram__bytes_read.sum + dram__bytes_write.sum,
 # a single pass) at the build named beside it by the digest of its source
-# files (profiles/glm_1m_last1024_filter_k_stream_ncu.txt gives the command).
+# files (profiles/glm_1m_slices_filter_k_stream_ncu.txt gives the command).
 # Reported as roofline.traffic only while the running library is that build;
 # otherwise the traffic is reported as null.
 FILTER_TRAFFIC = {"glm_1m": {"bytes": 1196557312 + 397560832, "build": "a16bbb981209"}}
