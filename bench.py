@@ -223,9 +223,10 @@ class ClockSampler:
                 pass
         return None
 
-    def stop(self, window=None):
+    def stop(self):
+        """End sampling; the samples, for summary() over one window or more."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return None
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -240,10 +241,19 @@ class ClockSampler:
             try:
                 rows.append({"t": self._when(parts[0]), "sm": float(parts[2]),
                              "max": float(parts[3]), "util": float(parts[5]), "hw": parts[7],
-                             "hwt": parts[8], "swt": parts[9], "pcap": parts[10]})
+                             "hwt": parts[8], "swt": parts[9], "pcap": parts[10],
+                             "watts": float(parts[4]) if parts[4] not in ("", "[N/A]") else None})
             except ValueError:
                 continue
         os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summary(rows, window=None):
+        """Median SM clock under load, the maximum clock and the throttle
+        reasons seen inside window (host time.time() bounds)."""
+        if rows is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         if window is not None:
             inside = [r for r in rows if r["t"] is not None and window[0] <= r["t"] <= window[1]]
             rows = inside or rows
@@ -255,9 +265,10 @@ class ClockSampler:
                           ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
             if any(r[key] == "Active" for r in busy):
                 reasons.append(name)
+        watts = [r["watts"] for r in busy if r["watts"] is not None]
         return {"sm_mhz": statistics.median(r["sm"] for r in busy),
                 "sm_max_mhz": max(r["max"] for r in busy), "reasons": reasons,
-                "samples": len(busy)}
+                "samples": len(busy), "power_w": statistics.median(watts) if watts else None}
 
 
 # ---- the CPU oracle (baseline arm and cpu_baseline) -------------------------------------
@@ -418,7 +429,6 @@ def gpu_arm(args, world, rank, local):
     if rank == 0:
         clocks.start()
     tm = time_steps(hk, case, t, ws, dev, args.steps, args.warmup, args.replay_group, world)
-    clk = clocks.stop(tm["wall"]) if rank == 0 else None
     idx, sc = tm["idx"], tm["scores"]
     ms_step = tm["ms_step"]
     phase_ms, replay_ms, select_ms = tm["phases_ms"], tm["replay_ms"], tm["select_ms"]
@@ -448,12 +458,18 @@ def gpu_arm(args, world, rank, local):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": case["dtype"], "data": "synthetic", "config": workload_config(case, world),
-            "clocks": clk, "gpu_launches": launches_per_step(case) * args.steps,
+            "clocks": None, "gpu_launches": launches_per_step(case) * args.steps,
             "roofline": roofline, "select_ms": select_ms, "phases_ms": phase_ms,
             "replay": replay, "peaks": pk}
 
     if not args.no_e2e:
         line["e2e"] = e2e(args, hk, case, dev, ws, world)
+    # clocks of the main timed region (and of the e2e loop, which runs next)
+    rows = clocks.stop() if rank == 0 else None
+    if rank == 0:
+        line["clocks"] = ClockSampler.summary(rows, tm["wall"])
+        if "e2e" in line:
+            line["e2e"]["clocks"] = ClockSampler.summary(rows, line["e2e"].pop("wall"))
     if not args.no_twopass:
         line["twopass"] = twopass(hk, case, t, dev, idx, pairs)
     if not args.no_sharded:
@@ -635,6 +651,8 @@ def e2e(args, hk, case, dev, ws, world):
     def compute(b):
         comp.wait_event(uploaded[b])
         comp.wait_event(downloaded[b])  # the results last in buffer b have left
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ev[0].record(comp)
         dv = dev_in[b]
         if case["dtype"] == "bf16":
             q = dv["q"].view(torch.int16).view(torch.bfloat16)
@@ -646,6 +664,8 @@ def e2e(args, hk, case, dev, ws, world):
                   k_scale=dv["k_scale"], scores=False, workspace=ws, out=(dev_idx[b], None))
         hk.replay(q, k, dv["w"], dev_idx[b], q_scale=dv["q_scale"], k_scale=dv["k_scale"],
                   out=dev_rs[b])
+        ev[1].record(comp)
+        compute_events.append(ev)
         computed[b].record(comp)
 
     def download(b):
@@ -665,15 +685,19 @@ def e2e(args, hk, case, dev, ws, world):
             download(b)
         torch.cuda.synchronize()
 
+    compute_events = []  # device time of each step's select + replay
     for e in computed + downloaded:
         e.record(comp)
     run(2)  # warm-up
     steps = max(10, min(args.steps, 20))  # pipeline fill and drain spread over 10+ steps
     barrier(world)
     gc.disable()  # no collector pause while the host issues the steps
+    compute_events.clear()
+    wall0 = time.time()
     t0 = time.perf_counter()
     run(steps)
     elapsed = time.perf_counter() - t0
+    wall1 = time.time()
     gc.enable()
     dt = max_over_ranks(elapsed / steps, world, dev)
     # the last step's results arrived whole
@@ -681,9 +705,12 @@ def e2e(args, hk, case, dev, ws, world):
         raise RuntimeError("e2e: downloaded indices differ from the device result")
     return {"value": sum_over_ranks(pairs_of(case), world, dev) / dt, "unit": "pairs/s",
             "ms_per_step": dt * 1e3,
+            # device time of the step's select + replay inside this loop (CUDA
+            # events on the compute stream, after its waits for the copies)
+            "compute_ms_per_step": statistics.mean(a.elapsed_time(b) for a, b in compute_events),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
             "copies": "own streams, double-buffered: next step's inputs up and this step's "
-                      "results down while a step computes"}
+                      "results down while a step computes", "wall": (wall0, wall1)}
 
 
 def twopass(hk, case, t, dev, idx_ref, pairs):
