@@ -268,7 +268,9 @@ class ClockSampler:
         watts = [r["watts"] for r in busy if r["watts"] is not None]
         return {"sm_mhz": statistics.median(r["sm"] for r in busy),
                 "sm_max_mhz": max(r["max"] for r in busy), "reasons": reasons,
-                "samples": len(busy), "power_w": statistics.median(watts) if watts else None}
+                "samples": len(busy),
+                # nvidia-smi's power.draw: the board's mean power over the last second
+                "power_w_1s_mean": statistics.median(watts) if watts else None}
 
 
 # ---- the CPU oracle (baseline arm and cpu_baseline) -------------------------------------

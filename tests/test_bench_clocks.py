@@ -36,7 +36,7 @@ def test_windows_split_the_samples(tmp_path):
     t = [r["t"] for r in rows]
     first = bench.ClockSampler.summary(rows, (t[0], t[1]))
     assert first["sm_mhz"] == 2070 and first["reasons"] == [] and first["samples"] == 2
-    assert abs(first["power_w"] - 955.25) < 1e-9
+    assert abs(first["power_w_1s_mean"] - 955.25) < 1e-9
     second = bench.ClockSampler.summary(rows, (t[2], t[4]))
     # the idle sample (utilisation 0) is left out of the median and the reasons
     assert second["samples"] == 2 and second["sm_mhz"] == 1897.5
