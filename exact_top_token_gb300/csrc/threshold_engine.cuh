@@ -407,12 +407,24 @@ __global__ void __launch_bounds__(kThreads, 2) k_threshold(const TArgs a) {
         stream::HeadSum<H> hs;
         hs.reset();
         float sc = 0.0f;
+        // the accumulator goes back to the MMA issuer as soon as its last
+        // columns are in registers, before they are reduced
+        auto release = [&]() {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(acc_empty + e_slot);
+          if (++e_slot == kSlots) {
+            e_slot = 0;
+            e_aphase ^= 1u;
+          }
+        };
         if constexpr (H >= 32) {
 #pragma unroll
           for (int c0 = 0; c0 < H; c0 += 32) {
             float v[32];
             tc::tmem_ld32(taddr + c0, v);
             tc::tmem_wait_ld(v);
+            if (c0 + 32 == H) release();
 #pragma unroll
             for (int h = 0; h < 32; h += 4) {
               const float4 w4 = *reinterpret_cast<const float4*>(wq + c0 + h);
@@ -425,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_threshold(const TArgs a) {
           float v[16];
           tc::tmem_ld16(taddr, v);
           tc::tmem_wait_ld(v);
+          release();
           if (H == 1) {
             sc = stream::single_head_score<H>(v[0], wq[0]);
           } else {
@@ -434,13 +447,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_threshold(const TArgs a) {
           }
         }
         sc = finish_score(sc, ks);
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(acc_empty + e_slot);
-        if (++e_slot == kSlots) {
-          e_slot = 0;
-          e_aphase ^= 1u;
-        }
         // rows past M (the last tile's padding) sort last
         tc::tmem_st1(kcol + (uint32_t)i, i * kTileKeys + row < q.M ? desc32(sc) : 0xffffffffu);
       }
