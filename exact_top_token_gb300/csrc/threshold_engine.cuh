@@ -13,8 +13,10 @@
 //                with cp.async into a ring of stages
 //   warp 12      TMEM allocator and MMA issuer (128 samples x max(H, 16))
 //   warps 8..11  epilogue (TMEM lane = sample): the head reduction of the
-//                filter, then the sample's ordered key desc32(score) stored
-//                into tensor memory, one column per tile
+//                filter (the accumulator handed back to the MMA issuer once
+//                its last columns are in registers), then the sample's
+//                ordered key desc32(score) stored into tensor memory, one
+//                column per tile
 //   warps 4..7   select: the r-th smallest key of the query's M keys, read
 //                back from tensor memory (radix select over 2048 bins that
 //                span the keys' own range, shared-memory histogram), while
