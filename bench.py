@@ -376,32 +376,19 @@ def workload_config(case, world=1):
 
 # ---- the GPU arm -------------------------------------------------------------------------
 
-def fallback_chunks(n, L, k_top, capacity=0):
-    """Score-table chunks of the fallback past 64 failed queries: the candidate
-    buffer and the recovery rows of the select workspace hold whole rows of L
-    scores (the library's workspace layout, 1 KiB-aligned buffers)."""
-    def al(x):
-        return (x + 1023) // 1024 * 1024
-    n_pad = (n + 511) // 512 * 512
-    C = capacity or 8 * k_top
-    rows = (al(n_pad * C * 8) + al(64 * L * 4)) // (L * 4)
-    if rows > 304:  # whole waves of the read-back's 304 CTAs, if no more chunks
-        waves = rows - rows % 304
-        if -(-n // waves) == -(-n // rows):
-            rows = waves
-    rows = min(rows, n)
-    return (n + rows - 1) // rows if n else 0
-
-
-def launches_per_step(case):
+def launches_per_step(hk, case):
     """Kernels of one step: select (rank, pack, [key-scale check], threshold,
     plan, filter, check, select, recovery, then per fallback chunk the table
     writer and the read-back, which return at once without a fallback) and
-    one replay launch."""
+    one replay launch. The chunk count is the library's own."""
     n, H, d = case["q"].shape
     L = case["k"].shape[0]
+    dt_code = hk.E4M3 if case["dtype"] == "e4m3" else hk.BF16
+    chunks = hk.select_fallback_chunks(n, L, H, d, case["k_top"], 0, dt_code)
+    if chunks < 0:
+        raise ValueError("unsupported shape")
     base = 9 if case["dtype"] == "e4m3" else 8
-    return base + 2 * fallback_chunks(n, L, case["k_top"]) + 1
+    return base + 2 * chunks + 1
 
 
 def gpu_arm(args, world, rank, local):
@@ -460,7 +447,7 @@ def gpu_arm(args, world, rank, local):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": case["dtype"], "data": "synthetic", "config": workload_config(case, world),
-            "clocks": None, "gpu_launches": launches_per_step(case) * args.steps,
+            "clocks": None, "gpu_launches": launches_per_step(hk, case) * args.steps,
             "roofline": roofline, "select_ms": select_ms, "phases_ms": phase_ms,
             "replay": replay, "peaks": pk}
 

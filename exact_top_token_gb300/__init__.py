@@ -17,6 +17,7 @@ import os
 from . import _build
 
 __all__ = ["build", "load", "select", "select_twopass", "replay", "select_workspace_size",
+           "select_fallback_chunks",
            "select_sharded", "select_varlen", "replay_varlen", "replay_backward",
            "replay_backward_varlen",
            "twopass_workspace_size", "sample_plan", "HytopkError", "STATUS", "PHASES", "Stats",
@@ -33,7 +34,8 @@ DEV_WAIT_TIMEOUT = 0x80000000  # a bounded wait gave up: the call's outputs are 
 BF16, E4M3, E4M3_BF16 = 0, 1, 2  # E4M3_BF16: e4m3 q (with q_scale), bf16 k
 
 # the C-ABI symbols declared in include/hytopk.h
-symbols = ("hytopk_select_workspace_size", "hytopk_select", "hytopk_select_ex", "hytopk_replay",
+symbols = ("hytopk_select_workspace_size", "hytopk_select_fallback_chunks", "hytopk_select",
+           "hytopk_select_ex", "hytopk_replay",
            "hytopk_twopass_workspace_size", "hytopk_select_twopass", "hytopk_select_noalloc",
            "hytopk_select_sharded_workspace_size", "hytopk_select_sharded",
            "hytopk_replay_backward", "hytopk_select_varlen_workspace_size",
@@ -81,6 +83,8 @@ def load(path: str | None = None):
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.hytopk_select_workspace_size.restype = Z
     lib.hytopk_select_workspace_size.argtypes = [I, I, I, I, I, I, I]
+    lib.hytopk_select_fallback_chunks.restype = ctypes.c_int32
+    lib.hytopk_select_fallback_chunks.argtypes = [I, I, I, I, I, I, I]
     sel = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, Z, P]
     lib.hytopk_select.restype = I
     lib.hytopk_select.argtypes = sel + [P]
@@ -196,6 +200,12 @@ def sample_plan(ctx: int, k_top: int):
 
 def select_workspace_size(n, L, H, d, k_top, capacity=0, dtype=BF16) -> int:
     return int(load().hytopk_select_workspace_size(n, L, H, d, k_top, capacity, dtype))
+
+
+def select_fallback_chunks(n, L, H, d, k_top, capacity=0, dtype=BF16) -> int:
+    """Score-table chunks (table writer + read-back launch pairs) of
+    hytopk_select's fallback; -1 for invalid arguments."""
+    return int(load().hytopk_select_fallback_chunks(n, L, H, d, k_top, capacity, dtype))
 
 
 def twopass_workspace_size(n, L, H, d, k_top, dtype=BF16, rows_per_chunk=0) -> int:

@@ -59,6 +59,20 @@ SelectLayout select_layout(int n, int L, int H, int d, int C, hytopk_dtype dt) {
 
 int default_capacity(int k_top, int capacity) { return capacity > 0 ? capacity : 8 * k_top; }
 
+// Rows per score-table chunk of the fallback past HYTOPK_MAX_RECOVERY_ROWS
+// failed queries: whole rows of L scores in the candidate and recovery-row
+// buffers (unused by then), in whole read-back waves (kTableCtas rows, one
+// per CTA) when that takes no more chunks (a chunk a few rows past a wave
+// leaves those rows to a second pass of the CTAs that took them).
+int fallback_chunk_rows(const SelectLayout& lay, int n, int L) {
+  size_t rows_fit = (lay.plan - lay.cand) / ((size_t)L * 4);
+  if (rows_fit > (size_t)kTableCtas) {
+    const size_t waves = rows_fit - rows_fit % kTableCtas;
+    if ((n + waves - 1) / waves == (n + rows_fit - 1) / rows_fit) rows_fit = waves;
+  }
+  return (int)(rows_fit < (size_t)n ? rows_fit : (size_t)n);
+}
+
 Problem make_problem(const void* q, const float* q_scale, const void* k, const float* k_scale,
                      const float* w, const int32_t* positions, int n, int L, int H, int d,
                      int k_top, hytopk_dtype dt) {
@@ -131,6 +145,16 @@ size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k_top, int c
   return select_layout(n, L, H, d, C, dt).total;
 }
 
+int32_t hytopk_select_fallback_chunks(int n, int L, int H, int d, int k_top, int capacity,
+                                      hytopk_dtype dt) {
+  if (check_shape(n, L, H, d, k_top, dt) != HYTOPK_OK) return -1;
+  const int C = default_capacity(k_top, capacity);
+  if (capacity < 0 || C < k_top) return -1;
+  if (n == 0) return 0;
+  const int rows = fallback_chunk_rows(select_layout(n, L, H, d, C, dt), n, L);
+  return rows > 0 ? (n + rows - 1) / rows : 0;
+}
+
 hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* k,
                                const float* k_scale, const float* w, const int32_t* positions,
                                int n, int L, int H, int d, int k_top, hytopk_dtype dt,
@@ -192,15 +216,7 @@ hytopk_status hytopk_select_ex(const void* q, const float* q_scale, const void* 
     // chunk by chunk. Whether that happens is known only on the device, so
     // these launches are always made and return at once without a fallback.
     float* table = reinterpret_cast<float*>(base + lay.cand);
-    // Chunks of whole read-back waves (kTableCtas rows, one per CTA) when
-    // that takes no more chunks: a chunk a few rows past a wave leaves those
-    // rows to a second pass of the CTAs that took them.
-    size_t rows_fit = (lay.plan - lay.cand) / ((size_t)L * 4);
-    if (rows_fit > (size_t)kTableCtas) {
-      const size_t waves = rows_fit - rows_fit % kTableCtas;
-      if ((n + waves - 1) / waves == (n + rows_fit - 1) / rows_fit) rows_fit = waves;
-    }
-    const int chunk = (int)(rows_fit < (size_t)n ? rows_fit : (size_t)n);
+    const int chunk = fallback_chunk_rows(lay, n, L);
     FallbackMaps maps;
     HYTOPK_TRY(prepare_fallback_table(p, ws, &maps));
     for (int slot0 = 0; chunk > 0 && slot0 < n; slot0 += chunk) {

@@ -170,6 +170,18 @@ HYTOPK_API int32_t hytopk_sample_plan(int64_t ctx, int32_t k_top, int32_t* posit
 HYTOPK_API size_t hytopk_select_workspace_size(int n, int L, int H, int d, int k_top, int capacity,
                                     hytopk_dtype dt);
 
+/* Score-table chunks of hytopk_select's fallback (HyScale explainer, HyTopK
+ * paragraph: past 64 failed queries every query is rescored). The fallback
+ * writes whole rows of L scores into the candidate and recovery-row buffers
+ * of the workspace and reads them back chunk by chunk; since only the device
+ * knows whether it is needed, every call launches one table writer and one
+ * read-back per chunk, which return at once when no fallback is needed.
+ * Arguments as for hytopk_select_workspace_size. Returns the chunk count (0
+ * for n = 0), or -1 for invalid or unsupported arguments. Host-only: no CUDA
+ * call. */
+HYTOPK_API int32_t hytopk_select_fallback_chunks(int n, int L, int H, int d, int k_top,
+                                                 int capacity, hytopk_dtype dt);
+
 /* Exact top-k selection without a score table (HyTopK).
  *   idx_out    [n, k_top] int32: key positions, score descending then position
  *              ascending; a query with ctx = pos+1 < k_top has its ctx keys

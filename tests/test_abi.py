@@ -302,3 +302,42 @@ def test_noalloc_host_checks(lib):
     assert call(**dict(big, pos=None)) == 1
     assert call(**dict(big, k=P((1 << 20) + 8))) == 5
     assert call(**big) == 3
+
+
+def fallback_chunks_restated(n, L, k_top, capacity=0):
+    """The fallback's score-table chunks from the workspace layout: whole rows
+    of L fp32 scores in the candidate buffer (n padded to 512 queries x C
+    slots x 8 bytes) and the 64 recovery rows (64 x L x 4 bytes), each buffer
+    1 KiB aligned; rounded down to whole waves of the read-back's 304 CTAs
+    when that takes no more chunks."""
+    def al(x):
+        return (x + 1023) // 1024 * 1024
+    if n == 0:
+        return 0
+    n_pad = (n + 511) // 512 * 512
+    C = capacity or 8 * k_top
+    rows = (al(n_pad * C * 8) + al(64 * L * 4)) // (L * 4)
+    if rows > 304:
+        waves = rows - rows % 304
+        if -(-n // waves) == -(-n // rows):
+            rows = waves
+    rows = min(rows, n)
+    return -(-n // rows)
+
+
+def test_fallback_chunk_count(lib):
+    fc = lib.hytopk_select_fallback_chunks
+    # the workloads: 1M keys (26 chunks of 320 rows), 262,144 keys with
+    # 2048 queries (7 chunks of 304: one read-back wave each), 64K keys
+    assert fc(8192, 1 << 20, 64, 128, 2048, 0, 1) == 26
+    assert fc(2048, 1 << 18, 16, 64, 2048, 0, 0) == 7
+    assert fc(1024, 1 << 16, 32, 128, 2048, 0, 0) == 2
+    assert fc(0, 4096, 4, 64, 256, 0, 0) == 0
+    assert fc(64, 4096, 4, 64, 256, 100, 0) == -1  # capacity below k
+    assert fc(64, 4096, 3, 64, 256, 0, 0) == -1    # H unsupported
+    for n in (1, 63, 512, 700, 4097, 8192):
+        for L in (4096, 65537, 1 << 20):
+            for k_top, cap in ((256, 0), (2048, 0), (2048, 4096), (16384, 0)):
+                for H, d, dt in ((64, 128, 1), (16, 64, 0)):
+                    got = fc(n, L, H, d, k_top, cap, dt)
+                    assert got == fallback_chunks_restated(n, L, k_top, cap), (n, L, k_top, cap)
