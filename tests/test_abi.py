@@ -341,3 +341,17 @@ def test_fallback_chunk_count(lib):
                 for H, d, dt in ((64, 128, 1), (16, 64, 0)):
                     got = fc(n, L, H, d, k_top, cap, dt)
                     assert got == fallback_chunks_restated(n, L, k_top, cap), (n, L, k_top, cap)
+
+
+def test_bench_launch_count_per_step(lib):
+    """The bench's gpu_launches claim per step: 9 select kernels with e4m3
+    (8 with bf16: no key-scale check), 2 per fallback chunk, 1 replay."""
+    import numpy as np
+
+    import bench
+    glm = {"q": np.empty((8192, 64, 128), np.uint8), "k": np.empty((1 << 20, 128), np.uint8),
+           "k_top": 2048, "dtype": "e4m3"}
+    assert bench.launches_per_step(hk, glm) == 9 + 2 * 26 + 1
+    mixed = {"q": np.empty((1024, 32, 128), np.uint16), "k": np.empty((1 << 16, 128), np.uint16),
+             "k_top": 2048, "dtype": "bf16"}
+    assert bench.launches_per_step(hk, mixed) == 8 + 2 * 2 + 1
